@@ -1,0 +1,216 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test ties the oracle to something it does not compute itself: the
+explicit (non-absorbed) path the pages prove equal (Huny's Dev Blog "MLA
+아키텍처 해부", section 3 and section 5 case 4), torch's textbook
+scaled-dot-product attention on explicitly reconstructed keys and values,
+closed forms (one token, zero query), numpy reductions, and the rank bound of
+section 5 case 2. ``test_planted_mistakes_are_caught`` shows that each of five
+plausible mistakes planted in the oracle fails these pins.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle
+
+SCALE = 1.0 / math.sqrt(128 + 64)
+
+
+def f64(bits):
+    return mi.bf16_to_f32(bits).astype(np.float64)
+
+
+def sdpa_reference(inp, scale=SCALE):
+    """Textbook attention via torch SDPA on explicit K = c W_UK^T, V = c W_UV^T (fp64)."""
+    H, n_q = inp.H, inp.n_q
+    wk = torch.from_numpy(f64(inp.w_uk))  # [H, d_nope, d_c]
+    wv = torch.from_numpy(f64(inp.w_uv))  # [H, d_v, d_c]
+    qn = torch.from_numpy(f64(inp.q_nope))
+    qr = torch.from_numpy(f64(inp.q_rope))
+    outs, lses = [], []
+    for b in range(inp.B):
+        s0, s1 = int(inp.seq_off[b]), int(inp.seq_off[b + 1])
+        L = s1 - s0
+        cb = torch.from_numpy(f64(inp.c[s0:s1]))
+        kb = torch.from_numpy(f64(inp.kr[s0:s1]))
+        K = torch.einsum("sc,hic->hsi", cb, wk)                       # [H, L, d_nope]
+        key = torch.cat([K, kb.expand(H, L, kb.shape[1])], dim=-1)    # [H, L, 192]
+        V = torch.einsum("sc,hic->hsi", cb, wv)                       # [H, L, d_v]
+        q = torch.cat([qn[b], qr[b]], dim=-1).permute(1, 0, 2)        # [H, n_q, 192]
+        allowed = torch.arange(L)[None, :] <= (L - n_q + torch.arange(n_q))[:, None]  # [n_q, L]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q[None], key[None], V[None], attn_mask=allowed, scale=scale)[0]           # [H, n_q, d_v]
+        logits = torch.einsum("hjd,hsd->hjs", q, key) * scale
+        lse = torch.logsumexp(logits.masked_fill(~allowed, float("-inf")), dim=-1)    # [H, n_q]
+        outs.append(o.permute(1, 0, 2))
+        lses.append(lse.permute(1, 0))
+    out = torch.stack(outs).reshape(-1, wv.shape[1]).numpy()
+    lse = torch.stack(lses).reshape(-1).numpy()
+    return out, lse
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return mi.workload_inputs(1)
+
+
+@pytest.fixture(scope="module")
+def multitok():
+    # ragged contexts, two causal queries, several pages, a one-token-past-page tail
+    return mi.make_inputs(B=3, H=4, n_q=2, seq_lens=[5, 64, 130], seed=7)
+
+
+def test_absorbed_equals_explicit_tiny(tiny):
+    """Huny section 5 case 4: absorbed and explicit agree; the pages print ~1e-15."""
+    a = oracle.absorbed_f64(tiny)
+    e = oracle.explicit_f64(tiny)
+    assert np.abs(a["out"] - e["out"]).max() <= 1e-10
+    assert np.abs(a["lse"] - e["lse"]).max() <= 1e-10
+
+
+def test_absorbed_equals_explicit_logits_and_probs(multitok):
+    n_max = int(multitok.seq_lens.max())
+    e = oracle.explicit_f64(multitok, max_tokens=n_max)
+    for row in range(multitok.B * multitok.n_q * multitok.H):
+        a = oracle.absorbed_probs_f64(multitok, row)
+        n = len(a["logits"])
+        assert np.abs(a["logits"] - e["logits"][row, :n]).max() <= 1e-10
+        assert np.abs(a["probs"] - e["probs"][row, :n]).max() <= 1e-10
+        assert np.all(e["probs"][row, n:] == 0.0)
+
+
+@pytest.mark.parametrize("case", ["tiny", "multitok"])
+def test_oracle_matches_torch_sdpa(case, request):
+    """The oracle's result equals torch's textbook attention on explicit K, V."""
+    inp = request.getfixturevalue(case)
+    ref_out, ref_lse = sdpa_reference(inp)
+    a = oracle.absorbed_f64(inp)
+    e = oracle.explicit_f64(inp)
+    assert np.abs(a["out"] - ref_out).max() <= 1e-10
+    assert np.abs(e["out"] - ref_out).max() <= 1e-10
+    assert np.abs(a["lse"] - ref_lse).max() <= 1e-10
+
+
+def test_score_split_equals_concatenated_dot(multitok):
+    """Huny section 2.2 and section 5 case 3: q.k = q^C.k^C + q^R.k^R."""
+    row = 2 * multitok.H + 3  # b=1, j=0, h=3
+    b, j, h = 1, 0, 3
+    a = oracle.absorbed_probs_f64(multitok, row)
+    s0 = int(multitok.seq_off[b])
+    n = len(a["logits"])
+    K = oracle.explicit_keys_f64(multitok.c[s0:s0 + n], multitok.w_uk, h)      # [n, 128]
+    qn = f64(multitok.q_nope[b, j, h])
+    qr = f64(multitok.q_rope[b, j, h])
+    kr = f64(multitok.kr[s0:s0 + n])
+    concat = np.concatenate([K, kr], axis=1) @ np.concatenate([qn, qr])
+    assert np.abs(a["content"] - K @ qn).max() <= 1e-12 * max(1.0, np.abs(K @ qn).max())
+    assert np.abs(a["pos"] - kr @ qr).max() <= 1e-12 * max(1.0, np.abs(kr @ qr).max())
+    assert np.abs((a["content"] + a["pos"]) - concat).max() <= 1e-11
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 64, 65])
+def test_softmax_rows_sum_to_one(L):
+    """ikmyungterran guide section 1.4: the softmax weights of a row sum to 1."""
+    inp = mi.make_inputs(B=1, H=2, n_q=1, seq_lens=[L], seed=100 + L)
+    e = oracle.explicit_f64(inp, max_tokens=L)
+    assert np.abs(e["probs"].sum(axis=1) - 1.0).max() <= 1e-12
+    assert (e["probs"] >= 0).all()
+    for row in range(2):
+        a = oracle.absorbed_probs_f64(inp, row)
+        assert abs(a["probs"].sum() - 1.0) <= 1e-12
+
+
+def test_single_token_context_returns_its_latent():
+    """One cached token: the weight is exactly 1, so u is that latent."""
+    inp = mi.make_inputs(B=2, H=3, n_q=1, seq_lens=[1, 1], seed=3)
+    a = oracle.absorbed_f64(inp)
+    for b in range(2):
+        for h in range(3):
+            r = b * 3 + h
+            c0 = f64(inp.c[inp.seq_off[b]])
+            assert np.array_equal(a["u"][r], c0)
+            z0 = (a["q_abs"][r] @ np.concatenate([c0, f64(inp.kr[inp.seq_off[b]])])) * SCALE
+            assert abs(a["lse"][r] - z0) <= 1e-12 * max(1.0, abs(z0))
+            ref = f64(inp.w_uv[h]) @ c0
+            assert np.abs(a["out"][r] - ref).max() <= 1e-12
+
+
+def test_zero_query_averages_the_latents():
+    """q = 0 gives uniform weights: u = mean of the attended latents, lse = ln n."""
+    inp = mi.make_inputs(B=2, H=2, n_q=2, seq_lens=[7, 70], seed=5)
+    inp.q_nope[...] = 0
+    inp.q_rope[...] = 0
+    a = oracle.absorbed_f64(inp)
+    for b in range(2):
+        for j in range(2):
+            n = int(inp.seq_lens[b]) - 2 + j + 1
+            mean = f64(inp.c[inp.seq_off[b]: inp.seq_off[b] + n]).mean(axis=0)
+            for h in range(2):
+                r = (b * 2 + j) * 2 + h
+                assert np.abs(a["u"][r] - mean).max() <= 1e-12
+                assert abs(a["lse"][r] - math.log(n)) <= 1e-12
+
+
+def test_identity_absorption_is_single_head_attention():
+    """W_UK = [I_128 | 0]: the absorbed query is q^C padded with zeros, so the
+    result is textbook attention with keys [c[:, :128] ; k^R] and values W_UV c."""
+    inp = mi.make_inputs(B=1, H=1, n_q=1, seq_lens=[97], seed=11)
+    w = np.zeros((1, 128, 512), dtype=np.uint16)
+    w[0, np.arange(128), np.arange(128)] = 0x3F80  # bf16 1.0
+    inp.w_uk = w
+    a = oracle.absorbed_f64(inp)
+    c = torch.from_numpy(f64(inp.c))
+    key = torch.cat([c[:, :128], torch.from_numpy(f64(inp.kr))], dim=1)
+    V = c @ torch.from_numpy(f64(inp.w_uv[0])).T
+    q = torch.cat([torch.from_numpy(f64(inp.q_nope[0, 0, 0])), torch.from_numpy(f64(inp.q_rope[0, 0, 0]))])
+    o = torch.nn.functional.scaled_dot_product_attention(q[None, None], key[None], V[None], scale=SCALE)[0, 0]
+    assert np.abs(a["q_abs"][0, :128] - f64(inp.q_nope[0, 0, 0])).max() == 0.0
+    assert np.abs(a["q_abs"][0, 128:512]).max() == 0.0
+    assert np.abs(a["out"][0] - o.numpy()).max() <= 1e-10
+
+
+def test_reconstructed_keys_have_rank_at_most_d_c():
+    """Huny section 5 case 2 (d_c = 16 here): K = C W_UK^T has rank <= d_c."""
+    rng = np.random.default_rng(21)
+    c = mi.f32_to_bf16(rng.standard_normal((128, 16), dtype=np.float32))
+    w = mi.f32_to_bf16(rng.standard_normal((2, 64, 16), dtype=np.float32))
+    for h in range(2):
+        K = oracle.explicit_keys_f64(c, w, h)
+        assert K.shape == (128, 64)
+        assert np.abs(K - f64(c) @ f64(w[h]).T).max() <= 1e-12
+        assert np.linalg.matrix_rank(K) == 16
+
+
+def test_split_pieces_merge_to_the_unsplit_result(multitok):
+    """Log-sum-exp merge of per-range partials reproduces the whole softmax."""
+    rows = np.arange(multitok.B * multitok.n_q * multitok.H)
+    full = oracle.absorbed_f64(multitok)
+    one = oracle.split_partials_f64(multitok, [[0, 1 << 30]], rows)
+    assert np.abs(one["u"][:, 0] - full["u"]).max() <= 1e-12
+    assert np.abs(one["lse"][:, 0] - full["lse"]).max() <= 1e-12
+    pieces = [[0, 3], [3, 64], [64, 129], [129, 200], [500, 600]]
+    parts = oracle.split_partials_f64(multitok, pieces, rows)
+    assert np.isneginf(parts["lse"][:, 4]).all() and (parts["u"][:, 4] == 0).all()
+    merged = oracle.combine_f64(parts["u"], parts["lse"])
+    assert np.abs(merged["u"] - full["u"]).max() <= 1e-12
+    assert np.abs(merged["lse"] - full["lse"]).max() <= 1e-12
+
+
+def test_fp32_variant_tracks_fp64(tiny):
+    a = oracle.absorbed_f64(tiny)
+    f = oracle.absorbed_f32(tiny)
+    assert np.abs(f["out"] - a["out"]).max() <= 1e-4 * max(1.0, np.abs(a["out"]).max())
+    assert np.abs(f["lse"] - a["lse"]).max() <= 1e-4
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5])
+def test_planted_mistakes_are_caught(mutant, multitok):
+    """A copy of the oracle with one planted mistake must fail the SDPA pin."""
+    ref_out, ref_lse = sdpa_reference(multitok)
+    bad = oracle.mutant_absorbed_f64(mutant, multitok)
+    err = max(np.abs(bad["out"] - ref_out).max(), np.abs(bad["lse"] - ref_lse).max())
+    assert err > 1e-6, f"mutant {mutant} slipped through (err {err:g})"
