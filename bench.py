@@ -1,0 +1,376 @@
+"""Benchmark: MLA decode tokens/s and latent-KV HBM GB/s on one GB300.
+
+Default workload: DeepSeek-V3-shaped decode, B=32 sequences x context 4096,
+H=128 heads, page 64, one query token per sequence (seeded synthetic data,
+random weights). One step = mla_absorb_q -> mla_decode_paged -> mla_combine
+-> mla_out_proj for the whole batch; tokens/s = query tokens per step / step
+time. L2 is flushed (a 256 MiB write) between timed steps; each step is timed
+with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same per-GPU batch on its own GPU (replicas,
+weak scaling, no data-path collective); rank 0 prints one JSON line with the
+max-over-ranks time. ``--impl reference`` times the CPU oracle (fp32 absorbed
+loops) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+METRIC = "MLA decode tokens/s & latent-KV HBM GB/s (% of GB300 roofline), 1 GPU"
+UNIT = "tokens/s"
+WORKLOAD_INDEX = 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(inp, budget_s: float = 12.0, max_seqs: int | None = None):
+    """Time the oracle's fp32 absorbed path on whole sequences (all heads) of ``inp``."""
+    import oracle
+    oracle.build()
+    H, n_q = inp.H, inp.n_q
+    seqs_done, t_total, reps = 0, 0.0, 0
+    order = list(range(inp.B))
+    while t_total < budget_s and (max_seqs is None or seqs_done < max_seqs):
+        b = order[reps % inp.B]
+        rows = np.arange(b * n_q * H, (b + 1) * n_q * H, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.absorbed_f32(inp, rows)
+        t_total += time.perf_counter() - t0
+        seqs_done += 1
+        reps += 1
+    tokens = seqs_done * n_q
+    return {"value": tokens / t_total, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{seqs_done} whole sequences x {H} heads (fp32 absorbed loops, same workload)",
+            "seconds": round(t_total, 3)}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    inp = mi.workload_inputs(WORKLOAD_INDEX)
+    T = inp.B * inp.n_q
+    per_step = max(1, min(inp.B, 4))
+    times = []
+    steps = args.warmup + args.steps
+    import oracle
+    oracle.build()
+    for s in range(steps):
+        seqs = [(s * per_step + i) % inp.B for i in range(per_step)]
+        rows = np.concatenate([np.arange(b * inp.n_q * inp.H, (b + 1) * inp.n_q * inp.H) for b in seqs])
+        t0 = time.perf_counter()
+        oracle.absorbed_f32(inp, rows.astype(np.int64))
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+    tok = per_step * inp.n_q
+    value = tok * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(inp, None),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} whole sequences (all {inp.H} heads) per step of the "
+                                   f"B={inp.B} batch"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(inp, num_splits):
+    return {"workload": f"DeepSeek-V3-shaped MLA decode: B={inp.B} x context "
+                        f"{int(inp.seq_lens[0])}, H={inp.H}, d_c=512, d_r=64, page 64, n_q={inp.n_q}",
+            "batch": inp.B, "context": int(inp.seq_lens[0]), "heads": inp.H, "n_q": inp.n_q,
+            "page_size": 64, "num_splits": num_splits, "cache_bytes": int(inp.seq_lens.sum()) * 1152,
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+def run_ours(args):
+    import torch
+    import mla_latent_kv_paged_gb300 as mla
+
+    ws_, rank, local = dist_env()
+    dist = None
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.build()
+
+    inp = mi.workload_inputs(WORKLOAD_INDEX)
+    pg = mi.make_paged(inp, spare_pages=mi.WORKLOADS[WORKLOAD_INDEX].spare_pages)
+    T, H, B, n_q = inp.B * inp.n_q, inp.H, inp.B, inp.n_q
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q_nope = to_dev(inp.q_nope.reshape(T, H, -1))
+    q_rope = to_dev(inp.q_rope.reshape(T, H, -1))
+    w_uk, w_uv = to_dev(inp.w_uk), to_dev(inp.w_uv)
+    cache = to_dev(pg.cache)
+    bt = torch.from_numpy(pg.block_table).to(dev)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    G = mla.default_splits(n_q)
+    bufs = dict(q_abs=torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev),
+                workspace=torch.empty(mla.workspace_bytes(B, n_q, H, G), dtype=torch.uint8, device=dev),
+                u=torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+                lse=torch.empty((T, H), dtype=torch.float32, device=dev),
+                out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        q_abs = mla.absorb_q(q_nope, q_rope, w_uk, bufs["q_abs"])
+        if ev is not None:
+            ev[1].record(stream)
+        mla.decode_paged(q_abs, cache, bt, sl, n_q=n_q, num_splits=G, workspace=bufs["workspace"],
+                         err_word=err)
+        if ev is not None:
+            ev[2].record(stream)
+        mla.combine(bufs["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=bufs["u"], lse=bufs["lse"])
+        if ev is not None:
+            ev[3].record(stream)
+        mla.out_proj(bufs["u"], w_uv, bufs["out"])
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error word {int(err.item())}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        step(events[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    phase = np.array([[events[k][i].elapsed_time(events[k][i + 1]) for i in range(4)]
+                      for k in range(args.steps)])  # ms: absorb, decode, combine, out_proj
+    step_ms = phase.sum(axis=1)
+    total_ms = float(step_ms.sum())
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws_ * T * args.steps / (total_ms * 1e-3)
+
+    # ---------------------------------------------------------------- end to end
+    # Per step: the new queries, block table and context lengths go host->device
+    # from pinned memory; out and lse come back device->host. The latent cache
+    # and weights stay resident in HBM (the KV cache is device state).
+    h_qn = torch.from_numpy(inp.q_nope.reshape(T, H, -1).view(np.int16)).pin_memory()
+    h_qr = torch.from_numpy(inp.q_rope.reshape(T, H, -1).view(np.int16)).pin_memory()
+    h_bt = torch.from_numpy(pg.block_table).pin_memory()
+    h_sl = torch.from_numpy(inp.seq_lens).pin_memory()
+    h_out = torch.empty((T, H, 128), dtype=torch.int16).pin_memory()
+    h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    d_qn = torch.empty((T, H, 128), dtype=torch.int16, device=dev)
+    d_qr = torch.empty((T, H, 64), dtype=torch.int16, device=dev)
+    h2d = h_qn.numel() * 2 + h_qr.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        d_qn.copy_(h_qn, non_blocking=True)
+        d_qr.copy_(h_qr, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        sl.copy_(h_sl, non_blocking=True)
+        r = mla.decode_step(d_qn.view(torch.bfloat16), d_qr.view(torch.bfloat16), w_uk, w_uv, cache, bt,
+                            sl, n_q=n_q, num_splits=G, bufs=bufs, err_word=err)
+        h_out.copy_(r["out"].view(torch.int16), non_blocking=True)
+        h_lse.copy_(r["lse"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_total = sum(e2e_times)
+    if dist is not None:
+        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = ws_ * T * args.steps / e2e_total
+
+    if rank == 0:
+        hbm, tflops, src = peaks()
+        wb = mi.workload_bytes(inp)
+        dec_ms = float(phase[:, 1].mean())
+        dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
+        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+        traffic = None
+        tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
+        if os.path.exists(tpath):
+            try:
+                tj = json.load(open(tpath))
+                if tj.get("kernel_rev") == mla_kernel_rev():
+                    traffic = tj.get("bytes_per_launch")
+            except Exception:
+                traffic = None
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(inp, G),
+            "phases_us": {"absorb_q": 1e3 * float(phase[:, 0].mean()),
+                          "decode_paged": 1e3 * dec_ms,
+                          "combine": 1e3 * float(phase[:, 2].mean()),
+                          "out_proj": 1e3 * float(phase[:, 3].mean())},
+            "roofline": {"kernel": "mla_decode_paged (plan + split-KV decode kernels)", "bound": "hbm",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": traffic, "peak_source": src,
+                         "alg_bytes_per_launch": dec_bytes, "alg_flops_per_launch": wb["decode_flops"],
+                         "tflops_achieved": wb["decode_flops"] / (dec_ms * 1e-3) / 1e12,
+                         "tensor_peak_tflops": tflops},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 5 * args.steps,
+            "clocks": clk,
+            "wall_s_timed_region": wall,
+        }
+        if ws_ == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def mla_kernel_rev():
+    """A digest of the decode kernel sources, to tell whether stored counters are stale."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_latent_kv_paged_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith(("decode", "plan")) or name.endswith(".cuh"):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

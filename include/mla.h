@@ -1,0 +1,165 @@
+/*
+ * mla.h — C ABI of the GB300 (sm_103a) library for Multi-Head Latent
+ * Attention (MLA) decode with weight absorption over a paged latent cache.
+ *
+ * What the four calls compute (notation of Huny's Dev Blog "Multi-Head
+ * Latent Attention(MLA) 아키텍처 해부", sections 1-3):
+ *   mla_absorb_q      qt = q^C (W^UK)^T per head, the absorbed query      (section 3.1)
+ *   mla_decode_paged  z_s = (qt . c_s + q^R . k^R_s) / sqrt(d_nope + d_r)  (section 2.2, 3.1)
+ *                     partial softmax over page ranges, partial u = a C^KV (section 3.2)
+ *   mla_combine       log-sum-exp merge of the range partials -> u, lse
+ *   mla_out_proj      out = u W^UV per head                                (section 3.2)
+ * One decode step for a batch is: mla_absorb_q -> mla_decode_paged ->
+ * mla_combine -> mla_out_proj, all on one stream.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers, owned and allocated by the
+ *     caller; the library never allocates, frees or synchronises. Every call
+ *     only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns.
+ *   - bf16 tensors are passed as uint16_t* holding IEEE bfloat16 bit patterns.
+ *   - Tensors are dense, row-major, in the index order written beside each
+ *     argument, and every pointer must be 16-byte aligned.
+ *   - Supported shapes: d_nope = d_v = 128, d_r = 64, d_c = 512 (a cache row
+ *     holds d_c + d_r = 576 values), page_size = 64, 1 <= H <= 128,
+ *     n_q in {1, 2}, 1 <= B <= MLA_MAX_BATCH. Other values return
+ *     MLA_ERR_UNSUPPORTED_SHAPE without launching anything.
+ *   - Argument errors found on the host return a status before any launch.
+ *     A failed launch returns MLA_ERR_CUDA (cudaGetLastError is consumed).
+ *   - Errors that only the device can see (a context length out of range, a
+ *     page id outside [0, num_pages), a wait that timed out) are written as
+ *     the first nonzero mla_status into *err_word (a device int32 the caller
+ *     zeroes and reads after its own synchronisation). The kernels then clamp
+ *     the bad value and finish without faulting; the results are not valid.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+#define MLA_MAX_BATCH 4096
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,       /* null/misaligned pointer, negative size, bad count */
+    MLA_ERR_UNSUPPORTED_SHAPE = 2, /* dimension outside the supported set */
+    MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+    MLA_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    MLA_ERR_TIMEOUT = 5,           /* device: a bounded wait gave up */
+    MLA_ERR_BOUNDS = 6             /* device: seq_len or page id out of range */
+} mla_status;
+
+/* Human-readable name of a status code. Never NULL. */
+const char* mla_status_string(int status);
+
+/* MLA_ABI_VERSION of the loaded library. */
+int mla_abi_version(void);
+
+/* Bytes one token occupies in one layer's latent cache: (d_c + d_r) * 2.
+ * Huny's Dev Blog "MLA 아키텍처 해부", section 2.2: (512 + 64) * 2 = 1152. */
+size_t mla_cache_bytes_per_token(int d_c, int d_r);
+
+/* Bytes of one cache page: page_size * (d_c + d_r) * 2 (73,728 at 64 tokens). */
+size_t mla_page_bytes(int page_size, int d_c, int d_r);
+
+/* ------------------------------------------------------------------------
+ * mla_absorb_q — absorb W_UK into the per-head content query.
+ *   q_abs[t][h][c]       = sum_i q_nope[t][h][i] * w_uk[h][i][c]   (c < d_c)
+ *   q_abs[t][h][d_c + e] = q_rope[t][h][e]                         (e < d_r)
+ * Huny's Dev Blog, section 3.1 (qt = q^C (W_i^UK)^T); tbr8.org "DeepSeek MLA
+ * 深度解析", weight-absorption section. The positional query is already
+ * rotated by the caller and is copied unchanged. fp32 accumulation, bf16
+ * (round-to-nearest-even) output.
+ *   q_nope [T][H][d_nope] bf16, q_rope [T][H][d_r] bf16,
+ *   w_uk   [H][d_nope][d_c] bf16, q_abs [T][H][d_c + d_r] bf16 (output).
+ *   T >= 1 is the number of query rows (B * n_q). */
+mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
+                        uint16_t* q_abs, int T, int H, int d_nope, int d_r, int d_c, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Split-KV decode. The pages of all sequences, taken in sequence order, are
+ * cut into `num_splits` contiguous ranges of near-equal page count (range p
+ * covers global pages [floor(p*P/num_splits), floor((p+1)*P/num_splits)),
+ * P = total pages). One worker (a pair of CTAs on two SMs) processes one
+ * range for one query index j. Where a range crosses a sequence boundary it
+ * yields one partial per sequence it touches, so at most num_splits + B - 1
+ * partials exist. The split points depend only on seq_lens and num_splits,
+ * so results are bit-reproducible for the same arguments.
+ *
+ * mla_decode_default_splits: the num_splits that fills the current device
+ * (SM count / (2 * n_q)); returns a value >= 1, or -1 if no device.
+ *
+ * mla_decode_workspace_bytes: bytes of workspace needed by mla_decode_paged
+ * and read by mla_combine for these arguments (0 if they are invalid).
+ *
+ * Workspace layout (int32 unless noted; every block starts at a 256-byte
+ * aligned offset; I = num_splits + B):
+ *   hdr[64]                 hdr[0] = number of partials, hdr[1] = used splits,
+ *                           hdr[2] = total pages
+ *   range_item[num_splits+1] first partial index of each range
+ *   seq_item[B+1]           first partial index of each sequence (partials of
+ *                           sequence b are seq_item[b] .. seq_item[b+1]-1)
+ *   seq_len_eff[B]          the context lengths actually used (clamped)
+ *   item_seq[I], item_page0[I], item_page1[I]   sequence and page range
+ *   lse_part[I][n_q][H]     float, natural-log sum-exp of the range's scores
+ *   o_part[I][n_q][H][512]  float, the range's softmax-normalised sum of latents
+ */
+int mla_decode_default_splits(int n_q);
+size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);
+
+/* mla_decode_paged — scores of every head against the paged latent cache and
+ * softmax-weighted latent sums, one partial per (range piece, query, head).
+ * For sequence b with context L = seq_lens[b] (which INCLUDES its n_q new
+ * tokens), query j attends logical tokens s = 0 .. L - n_q + j, and
+ *   z_s = softmax_scale * sum_{e < 576} q_abs[b][j][h][e] * row_s[e]
+ *   row_s = cache[block_table[b][s / 64]][s % 64][0:576]
+ * (Huny's Dev Blog section 2.2: the cached row is c^KV (512) then the shared
+ * rotated k^R (64); section 3.1: scoring in latent space; ikmyungterran.us
+ * attention guide section 1.3: softmax(z / sqrt(d_k)); the pages give
+ * d_k = d_nope + d_r, so softmax_scale is normally 1/sqrt(192)). The value
+ * sum uses only the first 512 columns of each row. Unused block-table
+ * entries are never read; slack rows past L in a sequence's last page may
+ * hold any bits (NaN included) and never reach the result.
+ *   q_abs       [B][n_q][H][576] bf16 (from mla_absorb_q)
+ *   cache       [num_pages][page_size][576] bf16
+ *   block_table [B][max_pages_per_seq] int32 physical page ids
+ *   seq_lens    [B] int32, n_q <= L <= max_pages_per_seq * page_size
+ *   workspace   >= mla_decode_workspace_bytes(B, n_q, H, num_splits) bytes
+ *   err_word    device int32 or NULL (see the conventions above). */
+mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            int B, int n_q, int H, int num_pages, int page_size,
+                            int max_pages_per_seq, float softmax_scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, int32_t* err_word,
+                            void* stream);
+
+/* mla_combine — merge the range partials of each (sequence, query, head):
+ *   lse = ln sum_k exp(lse_k),  u = sum_k exp(lse_k - lse) * o_k
+ * (the flash-decoding merge; Huny's Dev Blog section 4 table names
+ * FlashDecoding as the decode technique). A partial with lse_k = -inf has
+ * weight 0.
+ *   workspace  as filled by mla_decode_paged with the same B, n_q, H, num_splits
+ *   u          [B][n_q][H][512] bf16 output (round-to-nearest-even)
+ *   lse        [B][n_q][H] float output (natural log), may be NULL */
+mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_splits,
+                       uint16_t* u, float* lse, void* stream);
+
+/* ------------------------------------------------------------------------
+ * mla_out_proj — up-project the latent output through W_UV per head:
+ *   out[t][h][v] = sum_c w_uv[h][v][c] * u[t][h][c]
+ * Huny's Dev Blog section 3.2 (u_i W_i^UV after aggregation). fp32
+ * accumulation, bf16 output.
+ *   u [T][H][d_c] bf16, w_uv [H][d_v][d_c] bf16, out [T][H][d_v] bf16. */
+mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
+                        int T, int H, int d_c, int d_v, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_GB300_H */

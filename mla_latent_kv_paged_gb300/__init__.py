@@ -1,0 +1,227 @@
+"""Python binding of the GB300 MLA latent-KV paged decode library.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of ``libmla_gb300.so`` (built in-tree from ``csrc/``). Tensors are
+torch tensors on the current CUDA device; the calls enqueue work on
+``torch.cuda.current_stream()`` (or the stream given) and return at once.
+There is no CPU path: if the library is missing, importing the functions
+below raises.
+
+The names follow the C ABI in ``include/mla.h``:
+  absorb_q      qt = q^C W_UK (per head), q^R copied to columns 512..575
+  decode_paged  split-KV scores and softmax-weighted latent sums over pages
+  combine       log-sum-exp merge of the split partials -> u, lse
+  out_proj      out = u W_UV (per head)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
+
+D_NOPE, D_R, D_C, D_V, PAGE = 128, 64, 512, 128, 64
+D_ROW = D_C + D_R
+DEFAULT_SCALE = 1.0 / math.sqrt(D_NOPE + D_R)
+
+STATUS = {
+    0: "MLA_OK",
+    1: "MLA_ERR_INVALID_ARG",
+    2: "MLA_ERR_UNSUPPORTED_SHAPE",
+    3: "MLA_ERR_WORKSPACE_TOO_SMALL",
+    4: "MLA_ERR_CUDA",
+    5: "MLA_ERR_TIMEOUT",
+    6: "MLA_ERR_BOUNDS",
+}
+
+EXPORTS = [
+    "mla_status_string", "mla_abi_version", "mla_cache_bytes_per_token", "mla_page_bytes",
+    "mla_absorb_q", "mla_decode_default_splits", "mla_decode_workspace_bytes",
+    "mla_decode_paged", "mla_combine", "mla_out_proj",
+]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded C library (ctypes). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing; run __graft_entry__.build() first")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.mla_status_string.restype = ctypes.c_char_p
+            L.mla_status_string.argtypes = [i]
+            L.mla_abi_version.restype = i
+            L.mla_cache_bytes_per_token.restype = sz
+            L.mla_cache_bytes_per_token.argtypes = [i, i]
+            L.mla_page_bytes.restype = sz
+            L.mla_page_bytes.argtypes = [i, i, i]
+            L.mla_absorb_q.restype = i
+            L.mla_absorb_q.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+            L.mla_decode_default_splits.restype = i
+            L.mla_decode_default_splits.argtypes = [i]
+            L.mla_decode_workspace_bytes.restype = sz
+            L.mla_decode_workspace_bytes.argtypes = [i, i, i, i]
+            L.mla_decode_paged.restype = i
+            L.mla_decode_paged.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
+            L.mla_combine.restype = i
+            L.mla_combine.argtypes = [vp, i, i, i, i, vp, vp, vp]
+            L.mla_out_proj.restype = i
+            L.mla_out_proj.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MlaError(status, where)
+
+
+def _bits(t):
+    """bf16 tensors are passed as their raw 16-bit patterns."""
+    import torch
+    assert t.dtype in (torch.bfloat16, torch.int16, torch.uint16), t.dtype
+    assert t.is_contiguous(), "tensors must be contiguous"
+    return t
+
+
+# ---------------------------------------------------------------- small helpers
+def cache_bytes_per_token(d_c: int = D_C, d_r: int = D_R) -> int:
+    return int(lib().mla_cache_bytes_per_token(d_c, d_r))
+
+
+def page_bytes(page_size: int = PAGE, d_c: int = D_C, d_r: int = D_R) -> int:
+    return int(lib().mla_page_bytes(page_size, d_c, d_r))
+
+
+def default_splits(n_q: int) -> int:
+    g = int(lib().mla_decode_default_splits(n_q))
+    if g < 1:
+        raise MlaError(4, "mla_decode_default_splits")
+    return g
+
+
+def workspace_bytes(B: int, n_q: int, H: int, num_splits: int) -> int:
+    n = int(lib().mla_decode_workspace_bytes(B, n_q, H, num_splits))
+    if n == 0:
+        raise MlaError(1, "mla_decode_workspace_bytes")
+    return n
+
+
+# ---------------------------------------------------------------- the four calls
+def absorb_q(q_nope, q_rope, w_uk, q_abs=None, stream=None):
+    """q_nope [T,H,128], q_rope [T,H,64], w_uk [H,128,512] (bf16) -> q_abs [T,H,576]."""
+    import torch
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    if q_abs is None:
+        q_abs = torch.empty((T, H, D_ROW), dtype=torch.bfloat16, device=q_nope.device)
+    st = lib().mla_absorb_q(_ptr(_bits(q_nope)), _ptr(_bits(q_rope)), _ptr(_bits(w_uk)),
+                            _ptr(_bits(q_abs)), T, H, q_nope.shape[-1], q_rope.shape[-1],
+                            w_uk.shape[-1], _stream(stream))
+    _check(st, "mla_absorb_q")
+    return q_abs
+
+
+def decode_paged(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
+                 softmax_scale: float = DEFAULT_SCALE, workspace=None, err_word=None, stream=None):
+    """Split-KV decode over the paged cache. Returns (workspace, num_splits).
+
+    q_abs [B*n_q, H, 576] (or [B, n_q, H, 576]), cache [num_pages, 64, 576],
+    block_table [B, max_pages] int32, seq_lens [B] int32 (contexts include the
+    n_q new tokens). The workspace holds the plan and the partials for
+    ``combine``.
+    """
+    import torch
+    B, max_pages = block_table.shape
+    H = q_abs.shape[-2]
+    num_pages, page_size = cache.shape[0], cache.shape[1]
+    if num_splits is None:
+        num_splits = default_splits(n_q)
+    need = workspace_bytes(B, n_q, H, num_splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_abs.device)
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    assert block_table.is_contiguous() and seq_lens.is_contiguous()
+    st = lib().mla_decode_paged(_ptr(_bits(q_abs)), _ptr(_bits(cache)), _ptr(block_table),
+                                _ptr(seq_lens), B, n_q, H, num_pages, page_size, max_pages,
+                                float(softmax_scale), num_splits, _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(err_word),
+                                _stream(stream))
+    _check(st, "mla_decode_paged")
+    return workspace, num_splits
+
+
+def combine(workspace, *, B: int, n_q: int, H: int, num_splits: int, u=None, lse=None, stream=None):
+    """Merge the partials in ``workspace`` -> u [B*n_q, H, 512] bf16, lse [B*n_q, H] float."""
+    import torch
+    dev = workspace.device
+    if u is None:
+        u = torch.empty((B * n_q, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B * n_q, H), dtype=torch.float32, device=dev)
+    st = lib().mla_combine(_ptr(workspace), B, n_q, H, num_splits, _ptr(_bits(u)), _ptr(lse),
+                           _stream(stream))
+    _check(st, "mla_combine")
+    return u, lse
+
+
+def out_proj(u, w_uv, out=None, stream=None):
+    """u [T,H,512], w_uv [H,128,512] (bf16) -> out [T,H,128]."""
+    import torch
+    T, H = u.shape[0], u.shape[1]
+    if out is None:
+        out = torch.empty((T, H, D_V), dtype=torch.bfloat16, device=u.device)
+    st = lib().mla_out_proj(_ptr(_bits(u)), _ptr(_bits(w_uv)), _ptr(_bits(out)), T, H,
+                            u.shape[-1], w_uv.shape[1], _stream(stream))
+    _check(st, "mla_out_proj")
+    return out
+
+
+def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int,
+                num_splits: int | None = None, softmax_scale: float = DEFAULT_SCALE,
+                bufs: dict | None = None, err_word=None, stream=None):
+    """One full decode step: absorb_q -> decode_paged -> combine -> out_proj.
+
+    ``bufs`` may hold preallocated q_abs, workspace, u, lse, out tensors.
+    Returns dict(q_abs, u, lse, out).
+    """
+    bufs = bufs or {}
+    B = block_table.shape[0]
+    T, H = q_nope.shape[0], q_nope.shape[1]
+    q_abs = absorb_q(q_nope, q_rope, w_uk, bufs.get("q_abs"), stream)
+    ws, g = decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=num_splits,
+                         softmax_scale=softmax_scale, workspace=bufs.get("workspace"),
+                         err_word=err_word, stream=stream)
+    u, lse = combine(ws, B=B, n_q=n_q, H=H, num_splits=g, u=bufs.get("u"), lse=bufs.get("lse"),
+                     stream=stream)
+    out = out_proj(u, w_uv, bufs.get("out"), stream)
+    return dict(q_abs=q_abs, u=u, lse=lse, out=out, workspace=ws, num_splits=g)

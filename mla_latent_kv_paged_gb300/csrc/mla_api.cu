@@ -1,0 +1,132 @@
+// C ABI entry points: argument validation on the host, then kernel launches on
+// the caller's stream. Nothing here allocates, frees or synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_internal.cuh"
+
+using namespace mla;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status launch_status(cudaError_t e) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+bool heads_ok(int H) { return H >= 1 && H <= kMaxHeads; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED_SHAPE: return "MLA_ERR_UNSUPPORTED_SHAPE";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_BOUNDS: return "MLA_ERR_BOUNDS";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+size_t mla_cache_bytes_per_token(int d_c, int d_r) {
+  if (d_c < 0 || d_r < 0) return 0;
+  return (size_t)(d_c + d_r) * 2u;
+}
+
+size_t mla_page_bytes(int page_size, int d_c, int d_r) {
+  if (page_size < 0) return 0;
+  return (size_t)page_size * mla_cache_bytes_per_token(d_c, d_r);
+}
+
+mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
+                        uint16_t* q_abs, int T, int H, int d_nope, int d_r, int d_c, void* stream) {
+  if (!q_nope || !q_rope || !w_uk || !q_abs) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_abs))
+    return MLA_ERR_INVALID_ARG;
+  if (T < 1) return MLA_ERR_INVALID_ARG;
+  if (d_nope != kDNope || d_r != kDR || d_c != kDC || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  return launch_status(launch_absorb_q(q_nope, q_rope, w_uk, q_abs, T, H, (cudaStream_t)stream));
+}
+
+int mla_decode_default_splits(int n_q) {
+  if (n_q < 1) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  int g = sms / (2 * n_q);
+  return g < 1 ? 1 : g;
+}
+
+size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits) {
+  if (B < 1 || B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H) || num_splits < 1) return 0;
+  return plan_layout(nullptr, B, n_q, H, num_splits, nullptr);
+}
+
+mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            int B, int n_q, int H, int num_pages, int page_size,
+                            int max_pages_per_seq, float softmax_scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, int32_t* err_word,
+                            void* stream) {
+  if (!q_abs || !cache || !block_table || !seq_lens || !workspace) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(block_table) || !aligned16(seq_lens) ||
+      !aligned16(workspace))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || num_pages < 1 || max_pages_per_seq < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H) || page_size != kPage)
+    return MLA_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
+    return MLA_ERR_UNSUPPORTED_SHAPE;
+  const size_t need = plan_layout(nullptr, B, n_q, H, num_splits, nullptr);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  Plan plan;
+  plan_layout(workspace, B, n_q, H, num_splits, &plan);
+  cudaStream_t s = (cudaStream_t)stream;
+  mla_status st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq,
+                                            num_pages, num_splits, plan, err_word, s));
+  if (st != MLA_OK) return st;
+  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages,
+                                     max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
+}
+
+mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_splits, uint16_t* u,
+                       float* lse, void* stream) {
+  if (!workspace || !u) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned16(u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  Plan plan;
+  plan_layout(const_cast<void*>(workspace), B, n_q, H, num_splits, &plan);
+  return launch_status(launch_combine(plan, B, n_q, H, u, lse, (cudaStream_t)stream));
+}
+
+mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
+                        int d_c, int d_v, void* stream) {
+  if (!u || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (T < 1) return MLA_ERR_INVALID_ARG;
+  if (d_c != kDC || d_v != kDV || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  return launch_status(launch_out_proj(u, w_uv, out, T, H, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,102 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDNope = 128;
+constexpr int kDR = 64;
+constexpr int kDC = 512;
+constexpr int kDV = 128;
+constexpr int kRow = kDC + kDR;  // 576 values per cached token
+constexpr int kPage = 64;
+constexpr int kMaxHeads = 128;
+
+// ---------------------------------------------------------------- workspace
+// Views into the caller's workspace; the layout is documented in mla.h.
+struct Plan {
+  int32_t* hdr;          // [64]
+  int32_t* range_item;   // [G + 1]
+  int32_t* seq_item;     // [B + 1]
+  int32_t* seq_len_eff;  // [B]
+  int32_t* item_seq;     // [I]
+  int32_t* item_page0;   // [I]
+  int32_t* item_page1;   // [I]
+  float* lse_part;       // [I][n_q][H]
+  float* o_part;         // [I][n_q][H][512]
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Returns the total size; fills `p` relative to `base` when base != nullptr.
+__host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H, int G, Plan* p) {
+  const size_t I = (size_t)G + (size_t)B;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  size_t o_hdr = take(64 * 4);
+  size_t o_ri = take((size_t)(G + 1) * 4);
+  size_t o_si = take((size_t)(B + 1) * 4);
+  size_t o_sl = take((size_t)B * 4);
+  size_t o_is = take(I * 4);
+  size_t o_p0 = take(I * 4);
+  size_t o_p1 = take(I * 4);
+  size_t o_lse = take(I * n_q * H * 4);
+  size_t o_o = take(I * n_q * H * (size_t)kDC * 4);
+  if (base && p) {
+    char* c = reinterpret_cast<char*>(base);
+    p->hdr = reinterpret_cast<int32_t*>(c + o_hdr);
+    p->range_item = reinterpret_cast<int32_t*>(c + o_ri);
+    p->seq_item = reinterpret_cast<int32_t*>(c + o_si);
+    p->seq_len_eff = reinterpret_cast<int32_t*>(c + o_sl);
+    p->item_seq = reinterpret_cast<int32_t*>(c + o_is);
+    p->item_page0 = reinterpret_cast<int32_t*>(c + o_p0);
+    p->item_page1 = reinterpret_cast<int32_t*>(c + o_p1);
+    p->lse_part = reinterpret_cast<float*>(c + o_lse);
+    p->o_part = reinterpret_cast<float*>(c + o_o);
+  }
+  return off;
+}
+
+// ---------------------------------------------------------------- device helpers
+__device__ inline void report_error(int32_t* err_word, int code) {
+  if (err_word) atomicCAS(err_word, 0, code);
+}
+
+__device__ inline float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ inline float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ inline float bf16_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// float -> bf16 round-to-nearest-even (finite inputs; NaN stays NaN).
+__device__ inline uint16_t float_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+__device__ inline uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
+                        int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
+                        cudaStream_t s);
+cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
+                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
+                          const Plan& plan, int32_t* err_word, cudaStream_t s);
+cudaError_t launch_combine(const Plan& plan, int B, int n_q, int H, uint16_t* u, float* lse,
+                           cudaStream_t s);
+cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
+                            uint16_t* q_abs, int T, int H, cudaStream_t s);
+cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
+                            cudaStream_t s);
+
+}  // namespace mla

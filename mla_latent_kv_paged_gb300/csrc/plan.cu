@@ -1,0 +1,187 @@
+// Split-KV work plan: cuts the pages of all sequences (in sequence order) into
+// G contiguous ranges of near-equal size and lists the (sequence, page range)
+// pieces each range covers. Flash-decoding over a paged cache: the Huny's Dev
+// Blog "MLA 아키텍처 해부" section 4 table names FlashDecoding / PagedAttention
+// as the decode techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
+//
+// One block of 1024 threads. Integer work only; the output is a pure function
+// of (seq_lens, n_q, max_pages, G), so repeated calls give identical plans.
+#include "mla_internal.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive scan of v[0..n) in place (shared memory), returns the total.
+// Every thread of the block must call it.
+__device__ int block_exclusive_scan(int* v, int n, int* warp_sums) {
+  const int tid = threadIdx.x;
+  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int local = 0;
+  for (int i = lo; i < hi; ++i) local += v[i];
+  // inclusive scan of `local` across the block
+  int x = local;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int excl = x - local + (warp > 0 ? warp_sums[warp - 1] : 0);
+  const int total = warp_sums[31];
+  for (int i = lo; i < hi; ++i) {
+    int t = v[i];
+    v[i] = excl;
+    excl += t;
+  }
+  __syncthreads();
+  return total;
+}
+
+__device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table, int B,
+            int n_q, int max_pages, int num_pages, int G, Plan plan, int32_t* err_word) {
+  extern __shared__ int smem_i[];
+  int* s_pstart = smem_i;            // [B+1] exclusive page prefix
+  int* s_istart = smem_i + (B + 1);  // [B+1] exclusive piece prefix
+  __shared__ int warp_sums[32];
+  __shared__ int s_items;
+  const int tid = threadIdx.x;
+
+  // 1. clamp context lengths, count pages
+  for (int b = tid; b < B; b += kPlanThreads) {
+    int L = seq_lens[b];
+    if (L < n_q) {
+      report_error(err_word, MLA_ERR_BOUNDS);
+      L = n_q;
+    }
+    if (L > max_pages * kPage) {
+      report_error(err_word, MLA_ERR_BOUNDS);
+      L = max_pages * kPage;
+    }
+    plan.seq_len_eff[b] = L;
+    s_pstart[b] = (L + kPage - 1) / kPage;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(s_pstart, B, warp_sums);
+  if (tid == 0) {
+    s_pstart[B] = total;
+  }
+  __syncthreads();
+  const int Ge = min(G, total);  // >= 1 since every sequence has >= 1 page
+
+  // 2. pieces per sequence: interior boundaries x_p = floor(p*total/Ge),
+  //    p in [1, Ge-1], strictly inside (P_b, E_b)
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int64_t Pb = s_pstart[b], Eb = s_pstart[b + 1];
+    int64_t lo = ceil_div64((Pb + 1) * Ge, total);
+    int64_t hi = ceil_div64(Eb * Ge, total) - 1;
+    lo = max(lo, (int64_t)1);
+    hi = min(hi, (int64_t)Ge - 1);
+    s_istart[b] = 1 + (int)max((int64_t)0, hi - lo + 1);
+  }
+  __syncthreads();
+  const int items = block_exclusive_scan(s_istart, B, warp_sums);
+  if (tid == 0) {
+    s_istart[B] = items;
+    s_items = items;
+    plan.hdr[0] = items;
+    plan.hdr[1] = Ge;
+    plan.hdr[2] = total;
+  }
+  __syncthreads();
+
+  // 3. write the pieces of each sequence
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int64_t Pb = s_pstart[b], Eb = s_pstart[b + 1];
+    int64_t lo = max(ceil_div64((Pb + 1) * Ge, total), (int64_t)1);
+    int64_t hi = min(ceil_div64(Eb * Ge, total) - 1, (int64_t)Ge - 1);
+    int k = s_istart[b];
+    int64_t start = Pb;
+    for (int64_t p = lo; p <= hi; ++p) {
+      const int64_t x = (p * total) / Ge;
+      plan.item_seq[k] = b;
+      plan.item_page0[k] = (int)(start - Pb);
+      plan.item_page1[k] = (int)(x - Pb);
+      ++k;
+      start = x;
+    }
+    plan.item_seq[k] = b;
+    plan.item_page0[k] = (int)(start - Pb);
+    plan.item_page1[k] = (int)(Eb - Pb);
+    plan.seq_item[b] = s_istart[b];
+  }
+  if (tid == 0) plan.seq_item[B] = s_items;
+
+  // 4. first piece of each range
+  for (int p = tid; p <= G; p += kPlanThreads) {
+    int r;
+    if (p == 0) {
+      r = 0;
+    } else if (p >= Ge) {
+      r = s_items;
+    } else {
+      const int64_t x = ((int64_t)p * total) / Ge;
+      // largest b with P_b <= x (P strictly increasing)
+      int lo = 0, hi = B - 1;
+      while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s_pstart[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;
+      const int64_t Pb = s_pstart[b];
+      if (x == Pb) {
+        r = s_istart[b];
+      } else {
+        const int64_t first = max(ceil_div64((Pb + 1) * Ge, total), (int64_t)1);
+        r = s_istart[b] + (int)(p - first + 1);
+      }
+    }
+    plan.range_item[p] = r;
+  }
+
+  // 5. every page id that will be read must name a page of the pool
+  for (int g = tid; g < total; g += kPlanThreads) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (s_pstart[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    const int id = block_table[(size_t)lo * max_pages + (g - s_pstart[lo])];
+    if (id < 0 || id >= num_pages) report_error(err_word, MLA_ERR_BOUNDS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
+                        int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
+                        cudaStream_t s) {
+  const size_t smem = (size_t)2 * (B + 1) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  plan_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, block_table, B, n_q, max_pages, num_pages, G,
+                                            plan, err_word);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

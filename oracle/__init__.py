@@ -36,6 +36,8 @@ PINS = {
     "split_partials_f64": "pinned: one piece equals the unsplit result; merge identity",
     "combine_f64": "pinned: merge of the pieces equals the unsplit absorbed result",
     "absorbed_f32": "baseline only (timed); agrees with the fp64 path to fp32 rounding",
+    "absorb_q_f64": "pinned: numpy matmul; equals the q_abs of absorbed_f64",
+    "out_proj_f64": "pinned: numpy matmul; W_UV applied to absorbed_f64's u gives its out",
 }
 
 
@@ -235,3 +237,30 @@ def absorbed_f32(inp, rows=None, scale=None):
     if rc != 0:
         raise ValueError("oracle: bad row")
     return dict(u=u, lse=lse, out=out)
+
+
+def absorb_q_f64(q_nope_bits, q_rope_bits, w_uk_bits):
+    """The absorption step alone: [T,H,d_nope] x [H,d_nope,d_c] -> [T,H,d_c+d_r] (fp64)."""
+    lib = _load()
+    qn = np.ascontiguousarray(q_nope_bits, dtype=np.uint16)
+    qr = np.ascontiguousarray(q_rope_bits, dtype=np.uint16)
+    wk = np.ascontiguousarray(w_uk_bits, dtype=np.uint16)
+    T, H, d_nope = qn.shape
+    d_r, d_c = qr.shape[-1], wk.shape[-1]
+    out = np.empty((T, H, d_c + d_r))
+    lib.mla_oracle_absorb_q_f64(_p(qn), _p(qr), _p(wk), ctypes.c_int64(T), ctypes.c_int(H),
+                                ctypes.c_int(d_nope), ctypes.c_int(d_r), ctypes.c_int(d_c), _p(out))
+    return out
+
+
+def out_proj_f64(u_bits, w_uv_bits):
+    """The up-projection step alone: [T,H,d_c] x [H,d_v,d_c] -> [T,H,d_v] (fp64)."""
+    lib = _load()
+    u = np.ascontiguousarray(u_bits, dtype=np.uint16)
+    wv = np.ascontiguousarray(w_uv_bits, dtype=np.uint16)
+    T, H, d_c = u.shape
+    d_v = wv.shape[1]
+    out = np.empty((T, H, d_v))
+    lib.mla_oracle_out_proj_f64(_p(u), _p(wv), ctypes.c_int64(T), ctypes.c_int(H), ctypes.c_int(d_c),
+                                ctypes.c_int(d_v), _p(out))
+    return out

@@ -448,3 +448,40 @@ int mla_oracle_absorbed_f32(const uint16_t* q_nope, const uint16_t* q_rope,
     }
     return bad ? -1 : 0;
 }
+
+/* ---------------------------------------------------------------- single steps */
+/* Absorption step alone (Huny section 3.1): q_abs[r][c] = sum_i q^C[r][i] W_UK[h][i][c]
+ * for c < d_c, then q^R copied to q_abs[r][d_c + e]. Rows r = t*H + h of a
+ * [T][H] query block. */
+int mla_oracle_absorb_q_f64(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
+                            int64_t T, int H, int d_nope, int d_r, int d_c, double* q_abs) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * H; ++r) {
+        int h = (int)(r % H);
+        const uint16_t* wk = w_uk + (int64_t)h * d_nope * d_c;
+        double* qa = q_abs + r * (d_c + d_r);
+        for (int cc = 0; cc < d_c; ++cc) qa[cc] = 0.0;
+        for (int i = 0; i < d_nope; ++i) {
+            double qi = bf(q_nope[r * d_nope + i]);
+            for (int cc = 0; cc < d_c; ++cc) qa[cc] += qi * bf(wk[(int64_t)i * d_c + cc]);
+        }
+        for (int e = 0; e < d_r; ++e) qa[d_c + e] = bf(q_rope[r * d_r + e]);
+    }
+    return 0;
+}
+
+/* Up-projection step alone (Huny section 3.2): out[r][i] = sum_c W_UV[h][i][c] u[r][c]. */
+int mla_oracle_out_proj_f64(const uint16_t* u, const uint16_t* w_uv, int64_t T, int H, int d_c,
+                            int d_v, double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * H; ++r) {
+        int h = (int)(r % H);
+        const uint16_t* wv = w_uv + (int64_t)h * d_v * d_c;
+        for (int i = 0; i < d_v; ++i) {
+            double acc = 0.0;
+            for (int cc = 0; cc < d_c; ++cc) acc += bf(wv[(int64_t)i * d_c + cc]) * bf(u[r * d_c + cc]);
+            out[r * d_v + i] = acc;
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,87 @@
+"""Shared helpers for the tests: device transfer of generator outputs and error metrics."""
+import numpy as np
+
+import mla_inputs as mi
+
+# Tolerances for floating-point parity (bf16 inputs, fp32 accumulation), applied
+# to out, u and lse: max |gpu - oracle| and sum|gpu - oracle| / sum|oracle|.
+MAX_ABS = 2e-2
+MEAN_REL = 5e-3
+
+
+def to_dev_bf16(bits: np.ndarray):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.cuda().view(torch.bfloat16)
+
+
+def to_dev_i32(a: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def dev_to_bits(t) -> np.ndarray:
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def dev_bf16_to_f64(t) -> np.ndarray:
+    return mi.bf16_to_f32(dev_to_bits(t)).astype(np.float64)
+
+
+def errors(gpu: np.ndarray, ref: np.ndarray):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    d = np.abs(gpu - ref)
+    return float(d.max()), float(d.sum() / max(np.abs(ref).sum(), 1e-300))
+
+
+def assert_close(gpu, ref, what: str, max_abs=MAX_ABS, mean_rel=MEAN_REL):
+    assert np.isfinite(gpu).all(), f"{what}: non-finite values"
+    ma, mr = errors(gpu, ref)
+    assert ma <= max_abs and mr <= mean_rel, f"{what}: max_abs {ma:.3e} mean_rel {mr:.3e}"
+    return ma, mr
+
+
+def device_inputs(inp, pg):
+    """Move one batch to the device: returns dict of torch tensors."""
+    T = inp.B * inp.n_q
+    return dict(
+        q_nope=to_dev_bf16(inp.q_nope.reshape(T, inp.H, -1)),
+        q_rope=to_dev_bf16(inp.q_rope.reshape(T, inp.H, -1)),
+        w_uk=to_dev_bf16(inp.w_uk),
+        w_uv=to_dev_bf16(inp.w_uv),
+        cache=to_dev_bf16(pg.cache),
+        block_table=to_dev_i32(pg.block_table),
+        seq_lens=to_dev_i32(inp.seq_lens),
+    )
+
+
+def plan_mirror(seq_lens, n_q, max_pages, G, page=64):
+    """Python statement of the split plan documented in include/mla.h (integer work):
+    pages of all sequences in order, cut at floor(p * P / G'), G' = min(G, P)."""
+    lens = np.clip(np.asarray(seq_lens, dtype=np.int64), n_q, max_pages * page)
+    pages = (lens + page - 1) // page
+    starts = np.concatenate([[0], np.cumsum(pages)])
+    P = int(starts[-1])
+    Ge = min(G, P)
+    cuts = sorted(set([(p * P) // Ge for p in range(Ge + 1)]))
+    items = []  # (seq, page0, page1)
+    seq_item = []
+    for b in range(len(lens)):
+        seq_item.append(len(items))
+        lo, hi = int(starts[b]), int(starts[b + 1])
+        bounds = [lo] + [x for x in cuts if lo < x < hi] + [hi]
+        for a, z in zip(bounds[:-1], bounds[1:]):
+            items.append((b, a - lo, z - lo))
+    seq_item.append(len(items))
+    range_item = []
+    glob_start = [int(starts[b]) + p0 for (b, p0, _) in items]
+    for p in range(G + 1):
+        if p >= Ge:
+            range_item.append(len(items))
+        else:
+            x = (p * P) // Ge
+            range_item.append(glob_start.index(x))
+    return dict(items=np.array(items, dtype=np.int64), seq_item=np.array(seq_item),
+                range_item=np.array(range_item), total=P, Ge=Ge, lens=lens)

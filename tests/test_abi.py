@@ -1,0 +1,155 @@
+"""The C-ABI library: it loads without a GPU, exports every declared symbol,
+rejects bad arguments on the host before any launch, and its closed-form
+size functions give the numbers printed on the pages. No compute call runs."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import mla_latent_kv_paged_gb300 as mla
+from tests.helpers import plan_mirror
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla.build()
+    return mla.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = declared_functions()
+    assert "mla_decode_paged" in decl and "mla_combine" in decl
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert set(mla.EXPORTS) <= set(decl)
+    assert lib.mla_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code, name in mla.STATUS.items():
+        assert lib.mla_status_string(code).decode() == name
+    assert lib.mla_status_string(99).decode() == "MLA_ERR_UNKNOWN"
+
+
+def golden():
+    rows = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "cache_sizes.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, val, unit, src = [x.strip() for x in line.split("|")]
+        rows[key] = float(val)
+    return rows
+
+
+def test_cache_size_numbers_from_the_pages(lib):
+    g = golden()
+    mla_b = lib.mla_cache_bytes_per_token(512, 64)
+    assert mla_b == g["mla_bytes_per_token_layer"] == 1152
+    assert mla_b // 2 == g["mla_values_per_token"]
+    mha_b = 2 * 128 * 128 * 2  # MHA cache formula 2 n_h d_h b at the V3 shape
+    assert mha_b == g["mha_bytes_per_token_layer"]
+    assert mha_b // 2 == g["mha_values_per_token"]
+    assert round(100 * (1 - mla_b / mha_b), 2) == g["mla_vs_mha_saving_pct"]
+    assert round(100 * (1 - mla_b / g["gqa8_bytes_per_token_layer"]), 2) == g["mla_vs_gqa8_saving_pct"]
+    assert round(100 * (mla_b / 2) / g["mha_values_per_token"], 2) == g["mla_fraction_pct"]
+    assert (mla_b / 2) / (2 * 128) == g["mla_equivalent_gqa_groups"]
+    assert 2 * 8 * 128 == g["gqa8_values_per_token"]
+    MiB = 1 << 20
+    assert mla_b * 8192 / MiB == g["mla_8k_per_layer"]
+    assert mha_b * 8192 / MiB == g["mha_8k_per_layer"]
+    assert g["gqa8_bytes_per_token_layer"] * 8192 / MiB == g["gqa8_8k_per_layer"]
+    assert g["mqa_bytes_per_token_layer"] * 8192 / MiB == g["mqa_8k_per_layer"]
+    assert 512 / (128 * 128) == g["latent_fraction_of_kv_dims"]
+    assert 2 * 40 * 128 == g["mha_dims_40_heads"]
+    assert lib.mla_page_bytes(16, 512, 64) * 80 == g["mla_block_bytes_v2_80_layers_block16"]
+    assert lib.mla_page_bytes(64, 512, 64) == 73728
+
+
+def test_workspace_size_query(lib):
+    n = lib.mla_decode_workspace_bytes(32, 1, 128, 76)
+    assert n >= (76 + 32) * 128 * 512 * 4
+    assert lib.mla_decode_workspace_bytes(0, 1, 128, 76) == 0
+    assert lib.mla_decode_workspace_bytes(32, 3, 128, 76) == 0
+    assert lib.mla_decode_workspace_bytes(32, 1, 129, 76) == 0
+    assert lib.mla_decode_workspace_bytes(32, 1, 128, 0) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned, never dereferenced address
+
+
+def test_host_validation_absorb_and_out_proj(lib):
+    p = FAKE
+    assert lib.mla_absorb_q(None, p, p, p, 4, 128, 128, 64, 512, None) == 1
+    assert lib.mla_absorb_q(p, p, p, p + 2, 4, 128, 128, 64, 512, None) == 1
+    assert lib.mla_absorb_q(p, p, p, p, 0, 128, 128, 64, 512, None) == 1
+    assert lib.mla_absorb_q(p, p, p, p, 4, 128, 64, 64, 512, None) == 2
+    assert lib.mla_absorb_q(p, p, p, p, 4, 256, 128, 64, 512, None) == 2
+    assert lib.mla_out_proj(p, None, p, 4, 128, 512, 128, None) == 1
+    assert lib.mla_out_proj(p, p, p, 4, 128, 256, 128, None) == 2
+    assert lib.mla_out_proj(p, p, p, 4, 128, 512, 64, None) == 2
+
+
+def test_host_validation_decode_and_combine(lib):
+    p = FAKE
+    ws = lib.mla_decode_workspace_bytes(2, 1, 16, 4)
+
+    def dec(**kw):
+        a = dict(q=p, cache=p, bt=p, sl=p, B=2, n_q=1, H=16, num_pages=8, page=64, maxp=4,
+                 scale=0.07, G=4, ws=p, wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_decode_paged(a["q"], a["cache"], a["bt"], a["sl"], a["B"], a["n_q"], a["H"],
+                                    a["num_pages"], a["page"], a["maxp"], a["scale"], a["G"],
+                                    a["ws"], a["wsb"], a["err"], None)
+
+    assert dec(q=None) == 1
+    assert dec(cache=p + 8) == 1
+    assert dec(B=0) == 1
+    assert dec(G=0) == 1
+    assert dec(scale=0.0) == 1
+    assert dec(scale=float("nan")) == 1
+    assert dec(num_pages=0) == 1
+    assert dec(n_q=3) == 2
+    assert dec(H=200) == 2
+    assert dec(page=16) == 2
+    assert dec(B=5000) == 2
+    assert dec(wsb=ws - 1) == 3
+    assert lib.mla_combine(None, 2, 1, 16, 4, p, p, None) == 1
+    assert lib.mla_combine(p, 2, 3, 16, 4, p, p, None) == 2
+    assert lib.mla_combine(p, 2, 1, 16, 4, p + 4, p, None) == 1
+
+
+@pytest.mark.parametrize("lens,G", [([256, 256], 76), ([4096] * 32, 76), ([64] * 3, 2),
+                                    ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5)])
+def test_plan_statement_covers_every_page_once(lens, G):
+    """The documented split plan: each range holds consecutive pages of near-equal
+    count; each sequence's pieces tile its pages in order."""
+    pl = plan_mirror(lens, 1, 200, G)
+    P, Ge = pl["total"], pl["Ge"]
+    pages = (np.asarray(lens) + 63) // 64
+    assert P == pages.sum() and Ge == min(G, P)
+    for b in range(len(lens)):
+        its = pl["items"][pl["seq_item"][b]:pl["seq_item"][b + 1]]
+        assert (its[:, 0] == b).all()
+        assert its[0, 1] == 0 and its[-1, 2] == pages[b]
+        assert (its[1:, 1] == its[:-1, 2]).all() and (its[:, 2] > its[:, 1]).all()
+    sizes = []
+    for p in range(G):
+        its = pl["items"][pl["range_item"][p]:pl["range_item"][p + 1]]
+        sizes.append(int((its[:, 2] - its[:, 1]).sum()) if len(its) else 0)
+    assert sum(sizes) == P
+    nz = [s for s in sizes if s]
+    assert max(nz) - min(nz) <= 1
+    assert len(pl["items"]) <= G + len(lens) - 1

@@ -1,0 +1,268 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI (GPU only).
+
+Floating-point results must agree with the oracle within max |err| <= 2e-2 and
+sum|err| / sum|ref| <= 5e-3 (bf16 inputs, fp32 accumulation); integer and
+indexing work (the split plan, page gathers, error words) must be bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+import oracle
+from tests.helpers import (assert_close, dev_bf16_to_f64, dev_to_bits, device_inputs, plan_mirror,
+                           to_dev_bf16, to_dev_i32)
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 1.0 / math.sqrt(192.0)
+
+
+@pytest.fixture(scope="module")
+def mla():
+    import mla_latent_kv_paged_gb300 as m
+    m.build()
+    return m
+
+
+def run_step(mla, inp, pg, num_splits=None, err=None):
+    import torch
+    d = device_inputs(inp, pg)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], d["block_table"],
+                        d["seq_lens"], n_q=inp.n_q, num_splits=num_splits, err_word=err)
+    torch.cuda.synchronize()
+    r["err"] = int(err.item())
+    return r
+
+
+def compare_full(inp, r, rows=None):
+    ref = oracle.absorbed_f64(inp, rows)
+    T, H = inp.B * inp.n_q, inp.H
+    sel = slice(None) if rows is None else rows
+    u = dev_bf16_to_f64(r["u"]).reshape(T * H, 512)[sel]
+    out = dev_bf16_to_f64(r["out"]).reshape(T * H, 128)[sel]
+    lse = r["lse"].double().cpu().numpy().reshape(T * H)[sel]
+    assert_close(u, ref["u"], "u")
+    assert_close(lse, ref["lse"], "lse")
+    return assert_close(out, ref["out"], "out")
+
+
+# ------------------------------------------------------------------ single steps
+@pytest.mark.parametrize("T,H", [(2, 16), (37, 128), (128, 128), (3, 5)])
+def test_absorb_q(mla, T, H):
+    rng = np.random.default_rng(T * 1000 + H)
+    qn = mi.f32_to_bf16(rng.standard_normal((T, H, 128), dtype=np.float32))
+    qr = mi.f32_to_bf16(rng.standard_normal((T, H, 64), dtype=np.float32))
+    wk = mi.f32_to_bf16(rng.standard_normal((H, 128, 512), dtype=np.float32) / np.float32(math.sqrt(512)))
+    ref = oracle.absorb_q_f64(qn, qr, wk)
+    q_abs = mla.absorb_q(to_dev_bf16(qn), to_dev_bf16(qr), to_dev_bf16(wk))
+    got_bits = dev_to_bits(q_abs)
+    assert np.array_equal(got_bits[..., 512:], qr)  # the rotated query is copied bit for bit
+    got = mi.bf16_to_f32(got_bits[..., :512]).astype(np.float64)
+    # one bf16 rounding of an fp32 sum: within 2^-8 relative plus fp32 noise
+    assert (np.abs(got - ref[..., :512]) <= np.abs(ref[..., :512]) * 2.0 ** -8 + 1e-5).all()
+
+
+@pytest.mark.parametrize("T,H", [(2, 16), (37, 128), (128, 128), (3, 5)])
+def test_out_proj(mla, T, H):
+    rng = np.random.default_rng(T * 7 + H)
+    u = mi.f32_to_bf16(rng.standard_normal((T, H, 512), dtype=np.float32) * np.float32(0.1))
+    wv = mi.f32_to_bf16(rng.standard_normal((H, 128, 512), dtype=np.float32) / np.float32(math.sqrt(512)))
+    ref = oracle.out_proj_f64(u, wv)
+    out = dev_bf16_to_f64(mla.out_proj(to_dev_bf16(u), to_dev_bf16(wv)))
+    assert (np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5).all()
+
+
+def test_combine_alone_merges_oracle_partials(mla):
+    """Feed oracle partials through the documented workspace layout into mla_combine."""
+    import torch
+    inp = mi.make_inputs(B=3, H=8, n_q=2, seq_lens=[70, 300, 129], seed=31)
+    G = 4
+    pl = plan_mirror(inp.seq_lens, inp.n_q, 8, G)
+    ws = torch.zeros(mla.workspace_bytes(inp.B, inp.n_q, inp.H, G), dtype=torch.uint8, device="cuda")
+    # fill seq_item and the partials at the documented offsets
+    I = G + inp.B
+    offs, off = [], 0
+    for nbytes in [64 * 4, (G + 1) * 4, (inp.B + 1) * 4, inp.B * 4, I * 4, I * 4, I * 4,
+                   I * inp.n_q * inp.H * 4, I * inp.n_q * inp.H * 512 * 4]:
+        offs.append(off)
+        off = (off + nbytes + 255) // 256 * 256
+    host = np.zeros(ws.numel(), dtype=np.uint8)
+    host[offs[2]:offs[2] + (inp.B + 1) * 4] = pl["seq_item"].astype(np.int32).view(np.uint8)
+    lse_part = np.full((I, inp.n_q, inp.H), -np.inf, dtype=np.float32)
+    o_part = np.zeros((I, inp.n_q, inp.H, 512), dtype=np.float32)
+    rows = np.arange(inp.B * inp.n_q * inp.H)
+    for k, (b, p0, p1) in enumerate(pl["items"]):
+        part = oracle.split_partials_f64(inp, [[p0 * 64, p1 * 64]], rows)
+        for j in range(inp.n_q):
+            r = (b * inp.n_q + j) * inp.H + np.arange(inp.H)
+            lse_part[k, j] = part["lse"][r, 0]
+            o_part[k, j] = part["u"][r, 0]
+    host[offs[7]:offs[7] + lse_part.nbytes] = lse_part.view(np.uint8).ravel()
+    host[offs[8]:offs[8] + o_part.nbytes] = o_part.view(np.uint8).ravel()
+    ws.copy_(torch.from_numpy(host))
+    u, lse = mla.combine(ws, B=inp.B, n_q=inp.n_q, H=inp.H, num_splits=G)
+    torch.cuda.synchronize()
+    ref = oracle.absorbed_f64(inp)
+    assert_close(dev_bf16_to_f64(u).reshape(-1, 512), ref["u"], "u", max_abs=1e-2, mean_rel=3e-3)
+    assert np.abs(lse.double().cpu().numpy().ravel() - ref["lse"]).max() <= 1e-5
+
+
+# ------------------------------------------------------------------ the decode path
+def test_tiny_workload_all_rows(mla):
+    inp = mi.workload_inputs(1)
+    pg = mi.make_paged(inp, spare_pages=4)
+    r = run_step(mla, inp, pg)
+    assert r["err"] == 0
+    compare_full(inp, r)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
+def test_ragged_multitoken_all_rows(mla, splits):
+    """Several pages, partial last pages, a 1-token sequence, causal pairs, any split count."""
+    inp = mi.make_inputs(B=5, H=128, n_q=2, seq_lens=[2, 64, 65, 300, 1000], seed=41)
+    pg = mi.make_paged(inp, spare_pages=3)
+    r = run_step(mla, inp, pg, num_splits=splits)
+    assert r["err"] == 0
+    compare_full(inp, r)
+
+
+@pytest.mark.parametrize("H", [1, 16, 100])
+def test_fewer_heads(mla, H):
+    inp = mi.make_inputs(B=3, H=H, n_q=1, seq_lens=[130, 64, 7], seed=43 + H)
+    pg = mi.make_paged(inp)
+    r = run_step(mla, inp, pg, num_splits=4)
+    assert r["err"] == 0
+    compare_full(inp, r)
+
+
+def test_full_step_matches_explicit_path(mla):
+    """Multi-token decode against the oracle's explicit (non-absorbed) K, V path."""
+    inp = mi.make_inputs(B=2, H=128, n_q=2, seq_lens=[333, 129], seed=45)
+    pg = mi.make_paged(inp)
+    r = run_step(mla, inp, pg)
+    e = oracle.explicit_f64(inp)
+    out = dev_bf16_to_f64(r["out"]).reshape(-1, 128)
+    assert_close(out, e["out"], "out vs explicit")
+
+
+def test_page_permutation_is_bit_exact(mla):
+    """The same logical cache in two different page layouts gives identical bits."""
+    inp = mi.make_inputs(B=4, H=128, n_q=1, seq_lens=[500, 64, 1, 257], seed=47)
+    r1 = run_step(mla, inp, mi.make_paged(inp, perm_seed=1, spare_pages=2))
+    r2 = run_step(mla, inp, mi.make_paged(inp, perm_seed=2, spare_pages=9))
+    for k in ["u", "out", "q_abs"]:
+        assert np.array_equal(dev_to_bits(r1[k]), dev_to_bits(r2[k])), k
+    assert np.array_equal(r1["lse"].cpu().numpy().view(np.uint32), r2["lse"].cpu().numpy().view(np.uint32))
+
+
+def test_plan_is_bit_exact(mla):
+    import torch
+    inp = mi.make_inputs(B=6, H=16, n_q=1, seq_lens=[1, 65, 130, 64, 1000, 63], seed=49)
+    pg = mi.make_paged(inp)
+    G = 5
+    r = run_step(mla, inp, pg, num_splits=G)
+    ws = r["workspace"].cpu().numpy()
+    B = inp.B
+    I = G + B
+
+    def i32(off, n):
+        return ws[off:off + 4 * n].view(np.int32)
+
+    offs, off = [], 0
+    for nbytes in [64 * 4, (G + 1) * 4, (B + 1) * 4, B * 4, I * 4, I * 4, I * 4]:
+        offs.append(off)
+        off = (off + nbytes + 255) // 256 * 256
+    pl = plan_mirror(inp.seq_lens, 1, pg.max_pages, G)
+    n = len(pl["items"])
+    hdr = i32(offs[0], 3)
+    assert list(hdr) == [n, pl["Ge"], pl["total"]]
+    assert np.array_equal(i32(offs[1], G + 1), pl["range_item"])
+    assert np.array_equal(i32(offs[2], B + 1), pl["seq_item"])
+    assert np.array_equal(i32(offs[3], B), inp.seq_lens)
+    assert np.array_equal(i32(offs[4], n), pl["items"][:, 0])
+    assert np.array_equal(i32(offs[5], n), pl["items"][:, 1])
+    assert np.array_equal(i32(offs[6], n), pl["items"][:, 2])
+
+
+def test_incremental_decode_matches_fresh(mla):
+    """Huny section 5 case 5: 8 prefill tokens, then 4 decode steps each appending
+    one latent; every step matches the oracle at that length, and decoding a
+    cache that already holds later tokens in its slack gives the same bits."""
+    import torch
+    full = mi.make_inputs(B=1, H=128, n_q=1, seq_lens=[12], seed=51)
+    pg_full = mi.make_paged(full, spare_pages=0)
+    d = device_inputs(full, pg_full)
+    for L in range(8, 13):
+        sub = mi.Inputs(B=1, H=128, n_q=1, seq_lens=np.array([L], np.int32),
+                        seq_off=np.array([0, L]), c=full.c[:L], kr=full.kr[:L], q_nope=full.q_nope,
+                        q_rope=full.q_rope, w_uk=full.w_uk, w_uv=full.w_uv)
+        pg_sub = mi.make_paged(sub, spare_pages=0)
+        r_fresh = run_step(mla, sub, pg_sub)
+        compare_full(sub, r_fresh)
+        sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+        r_grown = mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"],
+                                  d["block_table"], sl, n_q=1)
+        torch.cuda.synchronize()
+        for k in ["u", "out"]:
+            assert np.array_equal(dev_to_bits(r_fresh[k]), dev_to_bits(r_grown[k])), (L, k)
+
+
+def test_device_errors_are_reported_without_faulting(mla):
+    import torch
+    inp = mi.make_inputs(B=2, H=16, n_q=1, seq_lens=[100, 70], seed=53)
+    pg = mi.make_paged(inp)
+    d = device_inputs(inp, pg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # context longer than the block table row
+    sl = torch.tensor([100, 64 * pg.max_pages + 5], dtype=torch.int32, device="cuda")
+    mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], d["block_table"], sl,
+                    n_q=1, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 6
+    # a page id outside the pool
+    err.zero_()
+    bt = d["block_table"].clone()
+    bt[0, 0] = pg.num_pages + 3
+    mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], bt, d["seq_lens"],
+                    n_q=1, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 6
+    # the context still works afterwards
+    r = run_step(mla, inp, pg)
+    assert r["err"] == 0
+    compare_full(inp, r)
+
+
+# ------------------------------------------------------------------ full-size workloads
+SAMPLE = 24
+
+
+def sampled_rows(inp, n=SAMPLE, seed=0):
+    rng = np.random.default_rng(seed)
+    total = inp.B * inp.n_q * inp.H
+    rows = rng.choice(total, size=min(n, total), replace=False)
+    # always include the first and last rows (first/last sequence, head 0 / H-1)
+    return np.unique(np.concatenate([rows, [0, total - 1]])).astype(np.int64)
+
+
+@pytest.mark.parametrize("index", [2, 3, 4, 5])
+def test_full_size_workload_sampled(mla, index):
+    """Full-size workloads in the benchmark's launch configuration (default split
+    count), compared with the oracle on sampled rows."""
+    inp = mi.workload_inputs(index)
+    pg = mi.make_paged(inp, spare_pages=mi.WORKLOADS[index].spare_pages)
+    r = run_step(mla, inp, pg)
+    assert r["err"] == 0
+    rows = sampled_rows(inp, seed=index)
+    compare_full(inp, r, rows)
+    if index == 5:
+        e = oracle.explicit_f64(inp, rows[:4])
+        out = dev_bf16_to_f64(r["out"]).reshape(-1, 128)[rows[:4]]
+        assert_close(out, e["out"], "out vs explicit")
+    # every row is finite
+    assert np.isfinite(dev_bf16_to_f64(r["out"])).all()
+    assert np.isfinite(r["lse"].cpu().numpy()).all()

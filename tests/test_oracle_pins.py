@@ -214,3 +214,24 @@ def test_planted_mistakes_are_caught(mutant, multitok):
     bad = oracle.mutant_absorbed_f64(mutant, multitok)
     err = max(np.abs(bad["out"] - ref_out).max(), np.abs(bad["lse"] - ref_lse).max())
     assert err > 1e-6, f"mutant {mutant} slipped through (err {err:g})"
+
+
+def test_single_step_functions(tiny):
+    """The absorption and up-projection steps alone agree with numpy matmuls and
+    with the corresponding parts of the whole absorbed path."""
+    T = tiny.B * tiny.n_q
+    qn = tiny.q_nope.reshape(T, tiny.H, -1)
+    qr = tiny.q_rope.reshape(T, tiny.H, -1)
+    qa = oracle.absorb_q_f64(qn, qr, tiny.w_uk)
+    ref = np.einsum("thi,hic->thc", f64(qn), f64(tiny.w_uk))
+    assert np.abs(qa[..., :512] - ref).max() <= 1e-11
+    assert np.array_equal(qa[..., 512:], f64(qr))
+    full = oracle.absorbed_f64(tiny)
+    assert np.abs(qa.reshape(-1, 576) - full["q_abs"]).max() <= 1e-12
+    rng = np.random.default_rng(8)
+    u = mi.f32_to_bf16(rng.standard_normal((T, tiny.H, 512), dtype=np.float32))
+    o = oracle.out_proj_f64(u, tiny.w_uv)
+    assert np.abs(o - np.einsum("hvc,thc->thv", f64(tiny.w_uv), f64(u))).max() <= 1e-11
+    # W_UV applied to the absorbed path's own u reproduces its out
+    o_full = np.einsum("hvc,thc->thv", f64(tiny.w_uv), full["u"].reshape(T, tiny.H, 512))
+    assert np.abs(o_full.reshape(-1, 128) - full["out"]).max() <= 1e-11
