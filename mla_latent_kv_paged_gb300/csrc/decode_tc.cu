@@ -1,0 +1,571 @@
+// Split-KV MLA decode over the paged latent cache on the 5th-generation tensor
+// cores (tcgen05, sm_103a).
+//
+// What it computes (Huny's Dev Blog "MLA 아키텍처 해부", sections 2.2 and 3):
+// for one sequence b, query j and all heads h at once,
+//   z[h][s] = scale * q_abs[h] . row_s          (row_s = [c_s (512) ; k^R_s (64)])
+//   m, l    = running max / sum of exp over the tokens of a page range
+//   O[h]    = sum_s exp(z[h][s] - m) c_s        (u = a C^KV, before normalisation)
+// and writes o = O / l and lse = m + ln l for the range.
+//
+// Layout of the work. One worker = a cluster of two CTAs on two SMs; CTA r
+// owns the feature half r of every cache row: latent columns [256r, 256r+256)
+// and positional columns [512+32r, 512+32r+32). It TMA-loads only its half of
+// each 64-token page (36 KB), so every cached byte is read from HBM once.
+// Scores need all 576 columns, so each CTA computes a partial score
+// S_r[128 heads][64 tokens] (K = 288) with tcgen05 MMAs into tensor memory,
+// and the two CTAs swap partials through distributed shared memory (fp16,
+// 16 KB per page). Both then hold identical full scores, run the same online
+// softmax (one thread per head row), and each accumulates its own 256-column
+// half of O[128][512] in tensor memory with a second MMA (P[128][64] x
+// C[64][256]). The 128 heads share every page tile in shared memory, which
+// is the reuse the absorbed formulation creates.
+//
+// Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S double
+// buffer [256,384), the CTA's latent half of q_abs as the MMA A operand
+// [384,512). Shared memory: 4-stage page ring (147 KB), the positional half of
+// q_abs (2 x 8 KB), the peer's partial scores (2 x 16 KB), P (2 x 16 KB).
+//
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..5 = softmax
+// and epilogue, one thread per head row (TMEM lane). The softmax runs one
+// page behind the score MMAs so the partial-score exchange overlaps the next
+// page's MMAs.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include "mla_internal.cuh"
+#include "sm100.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16, 128B swizzle
+constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
+constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
+constexpr uint32_t kQkrBytes = 128 * 64;    // [128 heads][32] bf16, 64B swizzle
+constexpr uint32_t kXBytes = 8 * 128 * 16;  // peer partial scores: [8][128 heads] x 16 B (fp16)
+constexpr uint32_t kPBytes = 128 * 128;     // P [128 heads][64 tokens] bf16, 128B swizzle
+
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffQkr = kOffStage + kStages * kStageBytes;
+constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+
+// barrier indices
+enum {
+  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
+  SF0 = QCF + 1, SFREE0 = SF0 + 2, PF0 = SFREE0 + 2, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE0 = XF0 + 2,
+  OFREE = XE0 + 2, MMAD = OFREE + 1, kNumBars = MMAD + 1
+};
+constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffSlots + 16 + 1024;  // + alignment slack
+
+constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384, kTmCols = 512;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
+
+struct TileInfo {
+  int g;       // CTA-local tile counter
+  int item;    // partial index
+  int li;      // item counter within this worker
+  int first, last;
+  int tok0;    // first token of the page
+  int n_att;   // tokens this query attends
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_half2(uint32_t w) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
+                 const __grid_constant__ CUtensorMap map_qkr, const uint16_t* __restrict__ q_abs,
+                 const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, float sl2,
+                 Plan plan, int32_t* err_word) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  const int worker = blockIdx.x >> 1, j = blockIdx.y;
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlots);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffSlots + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(FULL0 + i), 1);
+      mbar_init(bar(EMPTY0 + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(QKRF0 + i), 1);
+      mbar_init(bar(QKRE0 + i), 1);
+      mbar_init(bar(SF0 + i), 1);
+      mbar_init(bar(SFREE0 + i), 128);
+      mbar_init(bar(PF0 + i), 128);
+      mbar_init(bar(PVD0 + i), 1);
+      mbar_init(bar(XF0 + i), 128);
+      mbar_init(bar(XE0 + i), 128);
+    }
+    mbar_init(bar(QCF), 128);
+    mbar_init(bar(OFREE), 128);
+    mbar_init(bar(MMAD), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_c);
+    prefetch_tmap(&map_kr);
+    prefetch_tmap(&map_qkr);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  const uint32_t tmem = *tmem_slot;
+  const int it0 = plan.range_item[worker], it1 = plan.range_item[worker + 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    int stage = 0;
+    uint32_t ph = 0;
+    int last_ph[kStages], last_qph[2] = {-1, -1};
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
+    bool ok = true;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int li = it - it0, qb = li & 1;
+      const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
+      if (!wait_phase(bar(QKRE0 + qb), ((li >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(QKRF0 + qb), kQkrBytes);
+        tma_load_2d(sbase + kOffQkr + qb * kQkrBytes, &map_qkr, bar(QKRF0 + qb), kDC + 32 * (int)rank,
+                    (b * n_q + j) * H, pol_keep);
+      }
+      last_qph[qb] = (li >> 1) & 1;
+      for (int pg = pg0; pg < pg1 && ok; pg += 32) {
+        const int mine = pg + lane;
+        const int id_l = mine < pg1 ? block_table[(size_t)b * max_pages + mine] : 0;
+        const int n = min(32, pg1 - pg);
+        for (int t = 0; t < n; ++t) {
+          const int pid = __shfl_sync(0xffffffffu, id_l, t);
+          if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
+          if (lane == 0) {
+            const uint32_t fb = bar(FULL0 + stage);
+            const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
+            mbar_arrive_expect_tx(fb, kStageBytes);
+            const int y = pid * kPage;
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb)
+              tma_load_2d(dst + cb * kCBoxBytes, &map_c, fb, 256 * (int)rank + 64 * cb, y, pol_stream);
+            tma_load_2d(dst + 4 * kCBoxBytes, &map_kr, fb, kDC + 32 * (int)rank, y, pol_stream);
+          }
+          last_ph[stage] = (int)ph;
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; ph ^= 1u; }
+        }
+      }
+    }
+    if (!ok) {
+      // let every issued copy land before this CTA can exit
+#pragma unroll
+      for (int i = 0; i < kStages + 2; ++i) {
+        const int ph_i = i < kStages ? last_ph[i] : last_qph[i - kStages];
+        const uint32_t b_i = i < kStages ? bar(FULL0 + i) : bar(QKRF0 + i - kStages);
+        if (ph_i >= 0) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(b_i, (uint32_t)ph_i) && clock64() - t0 < kWaitLimitCycles) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, 256, false, true);
+      int stage = 0;
+      uint32_t ph = 0;
+      int g = 0;
+      bool have_prev = false, ok = true;
+      int prev_g = 0, prev_stage = 0, prev_first = 0, prev_li = 0;
+
+      auto issue_pv = [&](int t, int st, int first, int li) -> bool {
+        const int pb = t & 1;
+        if (!wait_phase(bar(PF0 + pb), (t >> 1) & 1, abort_flag, err_word)) return false;
+        if (first && li > 0 && !wait_phase(bar(OFREE), (li - 1) & 1, abort_flag, err_word)) return false;
+        tc_fence_after();
+        const uint32_t pa = sbase + kOffP + pb * kPBytes;
+        const uint32_t sa = sbase + kOffStage + st * kStageBytes;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(sa + ks * 2048, kCBoxBytes, 1024, kSwizzle128B);
+          mma_ss(tmem + kTmO, ad, bd, kIdPV, (!first || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(PVD0 + pb));
+        mma_commit(bar(EMPTY0 + st));
+        return true;
+      };
+
+      for (int it = it0; it < it1 && ok; ++it) {
+        const int li = it - it0, qb = li & 1;
+        const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+        for (int i = 0; i < ntiles; ++i, ++g) {
+          if (i == 0) {
+            if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word) ||
+                !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          }
+          const int sb = g & 1;
+          if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
+              !wait_phase(bar(SFREE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
+          const uint32_t d = tmem + kTmS + 64 * sb;
+#pragma unroll
+          for (int ks = 0; ks < 16; ++ks) {
+            const uint64_t bd = smem_desc(sa + (ks >> 2) * kCBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128B);
+            mma_ts(d, tmem + kTmQ + ks * 8, bd, kIdQK, ks > 0 ? 1u : 0u);
+          }
+          const uint32_t qa = sbase + kOffQkr + qb * kQkrBytes;
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint64_t ad = smem_desc(qa + ks * 32, 16, 512, kSwizzle64B);
+            const uint64_t bd = smem_desc(sa + 4 * kCBoxBytes + ks * 32, 16, 512, kSwizzle64B);
+            mma_ss(d, ad, bd, kIdQK, 1u);
+          }
+          mma_commit(bar(SF0 + sb));
+          if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
+          if (have_prev && !issue_pv(prev_g, prev_stage, prev_first, prev_li)) { ok = false; break; }
+          have_prev = true;
+          prev_g = g;
+          prev_stage = stage;
+          prev_first = (i == 0);
+          prev_li = li;
+          if (++stage == kStages) { stage = 0; ph ^= 1u; }
+        }
+      }
+      if (ok && have_prev) issue_pv(prev_g, prev_stage, prev_first, prev_li);
+      mma_commit(bar(MMAD));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO, tQ = tmem + lane_off + kTmQ;
+    const uint32_t x_local = sbase + kOffX;
+    const uint32_t x_remote = mapa(x_local, peer);
+    const uint32_t xf_remote0 = mapa(bar(XF0), peer), xe_remote0 = mapa(bar(XE0), peer);
+    const int tid128 = threadIdx.x - 64;
+
+    auto load_qc = [&](int it) {
+      const int b = plan.item_seq[it];
+      const size_t qrow = ((size_t)b * n_q + j) * H + row;
+      const uint4* src = reinterpret_cast<const uint4*>(q_abs + qrow * kRow + 256 * rank);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 w = row < H ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
+          r[4 * v] = w.x; r[4 * v + 1] = w.y; r[4 * v + 2] = w.z; r[4 * v + 3] = w.w;
+        }
+        tmem_st32(tQ + 32 * c, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(QCF));
+    };
+
+    float s_prev[64];
+    TileInfo pv{};
+    bool have_prev = false, ok = true;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    // Finish tile t: merge the peer's partial, online softmax, P to smem,
+    // and for the last page of a range the normalised output.
+    auto finish = [&](const TileInfo& t) -> bool {
+      const int xb = t.g & 1;
+      if (!wait_phase(bar(XF0 + xb), (t.g >> 1) & 1, abort_flag, err_word, true)) return false;
+      const uint32_t xa = x_local + xb * kXBytes + (uint32_t)row * 16;
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        uint4 w;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(xa + q8 * 128 * 16));
+        const float2 a = unpack_half2(w.x), b2 = unpack_half2(w.y), c2 = unpack_half2(w.z), d2 = unpack_half2(w.w);
+        s_prev[8 * q8 + 0] += a.x; s_prev[8 * q8 + 1] += a.y;
+        s_prev[8 * q8 + 2] += b2.x; s_prev[8 * q8 + 3] += b2.y;
+        s_prev[8 * q8 + 4] += c2.x; s_prev[8 * q8 + 5] += c2.y;
+        s_prev[8 * q8 + 6] += d2.x; s_prev[8 * q8 + 7] += d2.y;
+      }
+      mbar_arrive_remote(xe_remote0 + 8u * xb);
+      // mask tokens past this query's causal limit
+      const int nv = t.n_att - t.tok0;  // valid tokens in this page (may be <= 0 or >= 64)
+      float mt = -INFINITY;
+#pragma unroll
+      for (int jj = 0; jj < 64; ++jj) {
+        if (jj >= nv) s_prev[jj] = -INFINITY;
+        mt = fmaxf(mt, s_prev[jj]);
+      }
+      bool need = false;
+      float alpha = 1.f;
+      if (t.first) {
+        m_run = mt;
+        l_run = 0.f;
+      } else if (mt > m_run + kRescaleThreshold) {
+        alpha = ex2(m_run - mt);
+        l_run *= alpha;
+        m_run = mt;
+        need = true;
+      }
+      if (__any_sync(0xffffffffu, need)) {
+        // O must hold every earlier page before it is rescaled
+        if (!wait_phase(bar(PVD0 + ((t.g - 1) & 1)), ((t.g - 1) >> 1) & 1, abort_flag, err_word)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 32 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 32; ++v) r[v] = __float_as_uint(__uint_as_float(r[v]) * alpha);
+          tmem_st32(tO + 32 * c, r);
+        }
+        tmem_wait_st();
+      }
+      // the P buffer of page t-2 must have been consumed
+      if (t.g >= 2 && !wait_phase(bar(PVD0 + xb), ((t.g >> 1) & 1) ^ 1, abort_flag, err_word)) return false;
+      uint32_t pw[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const float p0 = s_prev[2 * m] == -INFINITY ? 0.f : ex2(s_prev[2 * m] - m_run);
+        const float p1 = s_prev[2 * m + 1] == -INFINITY ? 0.f : ex2(s_prev[2 * m + 1] - m_run);
+        pw[m] = pack_bf16x2(p0, p1);
+        lsum += bf16_lo(pw[m]) + bf16_hi(pw[m]);
+      }
+      l_run += lsum;
+      const uint32_t prow = sbase + kOffP + xb * kPBytes + (uint32_t)row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t a = prow + (uint32_t)((c ^ (row & 7)) * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pw[4 * c]), "r"(pw[4 * c + 1]),
+                     "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(PF0 + xb));
+      if (t.last) {
+        if (!wait_phase(bar(PVD0 + xb), (t.g >> 1) & 1, abort_flag, err_word)) return false;
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const size_t orow = ((size_t)t.item * n_q + j) * H + row;
+        float4* dst = reinterpret_cast<float4*>(plan.o_part + orow * kDC + 256 * rank);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 32 * c, r);
+          tmem_wait_ld();
+          if (row < H) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[c * 8 + v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                           __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(OFREE));
+        if (rank == 0 && row < H)
+          plan.lse_part[orow] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      }
+      return true;
+    };
+
+    if (it0 < it1) load_qc(it0);
+    int g = 0;
+    int stage = 0;
+    for (int it = it0; it < it1 && ok; ++it) {
+      const int li = it - it0;
+      const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
+      const int L = plan.seq_len_eff[b];
+      const int n_att = L - n_q + j + 1;
+      const int ntiles = pg1 - pg0;
+      for (int i = 0; i < ntiles; ++i, ++g) {
+        const int sb = g & 1;
+        // scores of page g (this CTA's partial over its 288 columns)
+        if (!wait_phase(bar(SF0 + sb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+        tc_fence_after();
+        float s_cur[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tS + 64 * sb, r0);
+          tmem_ld32(tS + 64 * sb + 32, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 32; ++v) {
+            s_cur[v] = __uint_as_float(r0[v]) * sl2;
+            s_cur[32 + v] = __uint_as_float(r1[v]) * sl2;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(SFREE0 + sb));
+        const int tok0 = (pg0 + i) * kPage;
+        const int rows_valid = L - tok0;
+        if (rows_valid < kPage) {
+          // slack rows past the context may hold any bits: zero this CTA's latent
+          // half so 0-weight x NaN cannot reach O
+          const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
+          const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
+          for (int z = tid128; z < nz; z += 128) {
+            const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sa + cb * kCBoxBytes + rr * 128 + ch * 16),
+                         "r"(0u)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+        }
+        // send the partial to the peer (fp16, token pairs)
+        if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word, true)) { ok = false; break; }
+        {
+          const uint32_t xa = x_remote + sb * kXBytes + (uint32_t)row * 16;
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            uint4 w;
+            w.x = pack_half2(s_cur[8 * q8 + 0], s_cur[8 * q8 + 1]);
+            w.y = pack_half2(s_cur[8 * q8 + 2], s_cur[8 * q8 + 3]);
+            w.z = pack_half2(s_cur[8 * q8 + 4], s_cur[8 * q8 + 5]);
+            w.w = pack_half2(s_cur[8 * q8 + 6], s_cur[8 * q8 + 7]);
+            st_cluster_v4(xa + q8 * 128 * 16, w);
+          }
+          mbar_arrive_remote(xf_remote0 + 8u * sb);
+        }
+        // every score MMA of this range is done: stage the next range's query
+        if (i == ntiles - 1 && it + 1 < it1) load_qc(it + 1);
+        if (have_prev && !finish(pv)) { ok = false; break; }
+        pv = TileInfo{g, it, li, i == 0, i == ntiles - 1, tok0, n_att};
+#pragma unroll
+        for (int v = 0; v < 64; ++v) s_prev[v] = s_cur[v];
+        have_prev = true;
+        if (++stage == kStages) stage = 0;
+      }
+    }
+    if (ok && have_prev) finish(pv);
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (warp == 1 && lane == 0) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar(MMAD), 0) && clock64() - t0 < kWaitLimitCycles) {
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer has finished writing into this CTA's shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int decode_max_workers() {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return n;
+}
+
+cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
+                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
+                          const Plan& plan, int32_t* err_word, cudaStream_t s) {
+  CUtensorMap map_c, map_kr, map_qkr;
+  const uint64_t cache_rows = (uint64_t)num_pages * kPage;
+  const uint64_t q_rows = (uint64_t)B * n_q * H;
+  if (!make_map(&map_c, cache, kRow, cache_rows, kRow * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&map_kr, cache, kRow, cache_rows, kRow * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&map_qkr, q_abs, kRow, q_rows, kRow * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const float sl2 = scale * 1.4426950408889634f;
+  dim3 grid(2 * G, n_q, 1);
+  decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(map_c, map_kr, map_qkr, q_abs, block_table, n_q, H,
+                                                      max_pages, sl2, plan, err_word);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

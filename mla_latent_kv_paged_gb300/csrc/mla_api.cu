@@ -71,7 +71,10 @@ int mla_decode_default_splits(int n_q) {
     cudaGetLastError();
     return -1;
   }
-  int g = sms / (2 * n_q);
+  // one wave of worker clusters, shared by the n_q query indices
+  int workers = decode_max_workers();
+  if (workers < 1) workers = sms / 2;
+  int g = workers / n_q;
   return g < 1 ? 1 : g;
 }
 

@@ -92,6 +92,8 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
                           int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s);
+// Worker clusters (CTA pairs) of the decode kernel that fit on the device at once.
+int decode_max_workers();
 cudaError_t launch_combine(const Plan& plan, int B, int n_q, int H, uint16_t* u, float* lse,
                            cudaStream_t s);
 cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
