@@ -30,7 +30,6 @@
 // and epilogue, one thread per head row (TMEM lane). The softmax runs one
 // page behind the score MMAs so the partial-score exchange overlaps the next
 // page's MMAs.
-#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "mla_internal.cuh"
@@ -78,15 +77,6 @@ struct TileInfo {
   int n_att;   // tokens this query attends
 };
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-__device__ __forceinline__ float2 unpack_half2(uint32_t w) {
-  __half2 h = *reinterpret_cast<__half2*>(&w);
-  return __half22float2(h);
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
                  const __grid_constant__ CUtensorMap map_qkr, const uint16_t* __restrict__ q_abs,
@@ -114,14 +104,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_init(bar(SFREE0 + i), 128);
       mbar_init(bar(PF0 + i), 128);
       mbar_init(bar(PVD0 + i), 1);
-      mbar_init(bar(XF0 + i), 128);
-      mbar_init(bar(XE0 + i), 128);
+      mbar_init(bar(XF0 + i), 1);   // armed by this CTA, filled by the peer's st.async
+      mbar_init(bar(XE0 + i), 4);   // one arrive per softmax warp of the peer
     }
     mbar_init(bar(QCF), 128);
     mbar_init(bar(OFREE), 128);
     mbar_init(bar(MMAD), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // expect the peer's partial scores of this CTA's first two pages
+    mbar_arrive_expect_tx(bar(XF0), kXBytes);
+    mbar_arrive_expect_tx(bar(XF0 + 1), kXBytes);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_c);
@@ -197,28 +190,38 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Order: QK(g) then PV(g-2). Scores run two pages ahead of the value
+    // MMAs, so the tensor pipe has work while the softmax of page g-2 runs.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, 256, false, true);
+      // descriptor templates (start address added per use, in 16-byte units)
+      const uint64_t dQK_c = smem_desc(0, 16, 1024, kSwizzle128B);
+      const uint64_t dQK_r = smem_desc(0, 16, 512, kSwizzle64B);
+      const uint64_t dPV_a = smem_desc(0, 16, 1024, kSwizzle128B);
+      const uint64_t dPV_b = smem_desc(0, kCBoxBytes, 1024, kSwizzle128B);
+      // start-address field of a descriptor: 14 bits of (shared address >> 4);
+      // shared addresses can carry high bits that must not spill into the
+      // neighbouring fields
+      auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };
       int stage = 0;
       uint32_t ph = 0;
       int g = 0;
-      bool have_prev = false, ok = true;
-      int prev_g = 0, prev_stage = 0, prev_first = 0, prev_li = 0;
+      bool ok = true;
+      // pending value MMAs: (tile, stage, first-of-range, range counter)
+      int pq_t[3], pq_s[3], pq_f[3], pq_l[3];
+      int pq_head = 0, pq_n = 0;
 
       auto issue_pv = [&](int t, int st, int first, int li) -> bool {
         const int pb = t & 1;
         if (!wait_phase(bar(PF0 + pb), (t >> 1) & 1, abort_flag, err_word)) return false;
         if (first && li > 0 && !wait_phase(bar(OFREE), (li - 1) & 1, abort_flag, err_word)) return false;
         tc_fence_after();
-        const uint32_t pa = sbase + kOffP + pb * kPBytes;
-        const uint32_t sa = sbase + kOffStage + st * kStageBytes;
+        const uint64_t ad = dPV_a + da(sbase + kOffP + pb * kPBytes);
+        const uint64_t bd = dPV_b + da(sbase + kOffStage + st * kStageBytes);
+        mma_ss(tmem + kTmO, ad, bd, kIdPV, first ? 0u : 1u);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = smem_desc(pa + ks * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(sa + ks * 2048, kCBoxBytes, 1024, kSwizzle128B);
-          mma_ss(tmem + kTmO, ad, bd, kIdPV, (!first || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 1; ks < 4; ++ks) mma_ss(tmem + kTmO, ad + (ks * 32 >> 4), bd + (ks * 2048 >> 4), kIdPV, 1u);
         mma_commit(bar(PVD0 + pb));
         mma_commit(bar(EMPTY0 + st));
         return true;
@@ -236,32 +239,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
               !wait_phase(bar(SFREE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
+          const uint64_t bc = dQK_c + da(sbase + kOffStage + stage * kStageBytes);
           const uint32_t d = tmem + kTmS + 64 * sb;
+          mma_ts(d, tmem + kTmQ, bc, kIdQK, 0u);
 #pragma unroll
-          for (int ks = 0; ks < 16; ++ks) {
-            const uint64_t bd = smem_desc(sa + (ks >> 2) * kCBoxBytes + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-            mma_ts(d, tmem + kTmQ + ks * 8, bd, kIdQK, ks > 0 ? 1u : 0u);
-          }
-          const uint32_t qa = sbase + kOffQkr + qb * kQkrBytes;
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            const uint64_t ad = smem_desc(qa + ks * 32, 16, 512, kSwizzle64B);
-            const uint64_t bd = smem_desc(sa + 4 * kCBoxBytes + ks * 32, 16, 512, kSwizzle64B);
-            mma_ss(d, ad, bd, kIdQK, 1u);
-          }
+          for (int ks = 1; ks < 16; ++ks)
+            mma_ts(d, tmem + kTmQ + ks * 8, bc + (((ks >> 2) * kCBoxBytes + (ks & 3) * 32) >> 4), kIdQK, 1u);
+          const uint64_t ar = dQK_r + da(sbase + kOffQkr + qb * kQkrBytes);
+          const uint64_t br = dQK_r + da(sbase + kOffStage + stage * kStageBytes + 4 * kCBoxBytes);
+          mma_ss(d, ar, br, kIdQK, 1u);
+          mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
           mma_commit(bar(SF0 + sb));
           if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
-          if (have_prev && !issue_pv(prev_g, prev_stage, prev_first, prev_li)) { ok = false; break; }
-          have_prev = true;
-          prev_g = g;
-          prev_stage = stage;
-          prev_first = (i == 0);
-          prev_li = li;
+          const int slot = (pq_head + pq_n) % 3;
+          pq_t[slot] = g; pq_s[slot] = stage; pq_f[slot] = (i == 0); pq_l[slot] = li;
+          ++pq_n;
+          if (pq_n == 3) {
+            if (!issue_pv(pq_t[pq_head], pq_s[pq_head], pq_f[pq_head], pq_l[pq_head])) { ok = false; break; }
+            pq_head = (pq_head + 1) % 3;
+            --pq_n;
+          }
           if (++stage == kStages) { stage = 0; ph ^= 1u; }
         }
       }
-      if (ok && have_prev) issue_pv(prev_g, prev_stage, prev_first, prev_li);
+      while (ok && pq_n > 0) {
+        ok = issue_pv(pq_t[pq_head], pq_s[pq_head], pq_f[pq_head], pq_l[pq_head]);
+        pq_head = (pq_head + 1) % 3;
+        --pq_n;
+      }
       mma_commit(bar(MMAD));
     }
     __syncwarp();
@@ -300,32 +305,36 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     bool have_prev = false, ok = true;
     float m_run = -INFINITY, l_run = 0.f;
 
-    // Finish tile t: merge the peer's partial, online softmax, P to smem,
-    // and for the last page of a range the normalised output.
+    // Finish page t: merge the peer's partial, online softmax, P to shared
+    // memory, and for the last page of a range the normalised output.
     auto finish = [&](const TileInfo& t) -> bool {
       const int xb = t.g & 1;
-      if (!wait_phase(bar(XF0 + xb), (t.g >> 1) & 1, abort_flag, err_word, true)) return false;
+      if (!wait_phase(bar(XF0 + xb), (t.g >> 1) & 1, abort_flag, err_word)) return false;
+      if (tid128 == 0) mbar_arrive_expect_tx(bar(XF0 + xb), kXBytes);  // arm for page t+2
       const uint32_t xa = x_local + xb * kXBytes + (uint32_t)row * 16;
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
         uint4 w;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(xa + q8 * 128 * 16));
-        const float2 a = unpack_half2(w.x), b2 = unpack_half2(w.y), c2 = unpack_half2(w.z), d2 = unpack_half2(w.w);
+        const float2 a = f16x2_to_f32(w.x), b2 = f16x2_to_f32(w.y), c2 = f16x2_to_f32(w.z), d2 = f16x2_to_f32(w.w);
         s_prev[8 * q8 + 0] += a.x; s_prev[8 * q8 + 1] += a.y;
         s_prev[8 * q8 + 2] += b2.x; s_prev[8 * q8 + 3] += b2.y;
         s_prev[8 * q8 + 4] += c2.x; s_prev[8 * q8 + 5] += c2.y;
         s_prev[8 * q8 + 6] += d2.x; s_prev[8 * q8 + 7] += d2.y;
       }
-      mbar_arrive_remote(xe_remote0 + 8u * xb);
-      // mask tokens past this query's causal limit
-      const int nv = t.n_att - t.tok0;  // valid tokens in this page (may be <= 0 or >= 64)
-      float mt = -INFINITY;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(xe_remote0 + 8u * xb);
+      // mask tokens past this query's causal limit (only on the last pages)
+      const int nv = t.n_att - t.tok0;
+      if (nv < 64) {
 #pragma unroll
-      for (int jj = 0; jj < 64; ++jj) {
-        if (jj >= nv) s_prev[jj] = -INFINITY;
-        mt = fmaxf(mt, s_prev[jj]);
+        for (int jj = 0; jj < 64; ++jj)
+          if (jj >= nv) s_prev[jj] = -INFINITY;
       }
+      float mt = s_prev[0];
+#pragma unroll
+      for (int jj = 1; jj < 64; ++jj) mt = fmaxf(mt, s_prev[jj]);
       bool need = false;
       float alpha = 1.f;
       if (t.first) {
@@ -354,24 +363,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       }
       // the P buffer of page t-2 must have been consumed
       if (t.g >= 2 && !wait_phase(bar(PVD0 + xb), ((t.g >> 1) & 1) ^ 1, abort_flag, err_word)) return false;
-      uint32_t pw[32];
+      const float mref = m_run == -INFINITY ? 0.f : m_run;  // all-masked page: every p is 0
       float lsum = 0.f;
-#pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const float p0 = s_prev[2 * m] == -INFINITY ? 0.f : ex2(s_prev[2 * m] - m_run);
-        const float p1 = s_prev[2 * m + 1] == -INFINITY ? 0.f : ex2(s_prev[2 * m + 1] - m_run);
-        pw[m] = pack_bf16x2(p0, p1);
-        lsum += bf16_lo(pw[m]) + bf16_hi(pw[m]);
-      }
-      l_run += lsum;
       const uint32_t prow = sbase + kOffP + xb * kPBytes + (uint32_t)row * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
+        uint32_t pw[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float p0 = ex2(s_prev[8 * c + 2 * v] - mref);
+          const float p1 = ex2(s_prev[8 * c + 2 * v + 1] - mref);
+          pw[v] = cvt_bf16x2(p0, p1);
+          lsum += bf16_lo(pw[v]) + bf16_hi(pw[v]);
+        }
         const uint32_t a = prow + (uint32_t)((c ^ (row & 7)) * 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pw[4 * c]), "r"(pw[4 * c + 1]),
-                     "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]),
+                     "r"(pw[3])
                      : "memory");
       }
+      l_run += lsum;
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(PF0 + xb));
@@ -412,20 +422,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       const int ntiles = pg1 - pg0;
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int sb = g & 1;
-        // scores of page g (this CTA's partial over its 288 columns)
+        // this CTA's partial scores of page g (its 288 columns), pre-scaled to log2 units
         if (!wait_phase(bar(SF0 + sb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
         tc_fence_after();
         float s_cur[64];
         {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tS + 64 * sb, r0);
-          tmem_ld32(tS + 64 * sb + 32, r1);
+          uint32_t r[32];
+          tmem_ld32(tS + 64 * sb, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 32; ++v) {
-            s_cur[v] = __uint_as_float(r0[v]) * sl2;
-            s_cur[32 + v] = __uint_as_float(r1[v]) * sl2;
-          }
+          for (int v = 0; v < 32; ++v) s_cur[v] = __uint_as_float(r[v]) * sl2;
+          tmem_ld32(tS + 64 * sb + 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 32; ++v) s_cur[32 + v] = __uint_as_float(r[v]) * sl2;
         }
         tc_fence_before();
         mbar_arrive(bar(SFREE0 + sb));
@@ -444,20 +454,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           }
           fence_proxy_async_smem();
         }
-        // send the partial to the peer (fp16, token pairs)
+        // send the partial to the peer (fp16 pairs), completing its barrier
         if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word, true)) { ok = false; break; }
         {
           const uint32_t xa = x_remote + sb * kXBytes + (uint32_t)row * 16;
+          const uint32_t xf = xf_remote0 + 8u * sb;
 #pragma unroll
           for (int q8 = 0; q8 < 8; ++q8) {
             uint4 w;
-            w.x = pack_half2(s_cur[8 * q8 + 0], s_cur[8 * q8 + 1]);
-            w.y = pack_half2(s_cur[8 * q8 + 2], s_cur[8 * q8 + 3]);
-            w.z = pack_half2(s_cur[8 * q8 + 4], s_cur[8 * q8 + 5]);
-            w.w = pack_half2(s_cur[8 * q8 + 6], s_cur[8 * q8 + 7]);
-            st_cluster_v4(xa + q8 * 128 * 16, w);
+            w.x = cvt_f16x2(s_cur[8 * q8 + 0], s_cur[8 * q8 + 1]);
+            w.y = cvt_f16x2(s_cur[8 * q8 + 2], s_cur[8 * q8 + 3]);
+            w.z = cvt_f16x2(s_cur[8 * q8 + 4], s_cur[8 * q8 + 5]);
+            w.w = cvt_f16x2(s_cur[8 * q8 + 6], s_cur[8 * q8 + 7]);
+            st_async_v4(xa + q8 * 128 * 16, w, xf);
           }
-          mbar_arrive_remote(xf_remote0 + 8u * sb);
         }
         // every score MMA of this range is done: stage the next range's query
         if (i == ntiles - 1 && it + 1 < it1) load_qc(it + 1);
