@@ -11,25 +11,30 @@
 // Layout of the work. One worker = a cluster of two CTAs on two SMs; CTA r
 // owns the feature half r of every cache row: latent columns [256r, 256r+256)
 // and positional columns [512+32r, 512+32r+32). It TMA-loads only its half of
-// each 64-token page (36 KB), so every cached byte is read from HBM once.
-// Scores need all 576 columns, so each CTA computes a partial score
-// S_r[128 heads][64 tokens] (K = 288) with tcgen05 MMAs into tensor memory,
-// and the two CTAs swap partials through distributed shared memory (fp16,
-// 16 KB per page). Both then hold identical full scores, run the same online
-// softmax (one thread per head row), and each accumulates its own 256-column
-// half of O[128][512] in tensor memory with a second MMA (P[128][64] x
-// C[64][256]). The 128 heads share every page tile in shared memory, which
-// is the reuse the absorbed formulation creates.
+// each 64-token page (36 KB), so every cached byte is read from HBM once. The
+// 128 heads share every page tile in shared memory (the reuse the absorbed
+// formulation creates).
+//
+// Scores need all 576 columns: each CTA computes a partial score
+// S_r[128 heads][64 tokens] (K = 288) with tcgen05 MMAs into tensor memory.
+// The softmax of a page is split by tokens: CTA r finishes tokens
+// [32r, 32r+32). It sends the partial scores of the other 32 tokens to the
+// peer (fp32, 16 KB, st.async into the peer's shared memory), adds the
+// peer's partial for its own tokens, and both CTAs exchange their page
+// maxima so they share one exact running maximum per head. Each CTA then
+// exponentiates its 32 tokens, writes its half of P[128][64] (bf16) into its
+// own and the peer's shared memory, and accumulates its 256-column half of
+// O[128][512] in tensor memory with the second MMA (P x C[64][256]).
 //
 // Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S double
 // buffer [256,384), the CTA's latent half of q_abs as the MMA A operand
 // [384,512). Shared memory: 4-stage page ring (147 KB), the positional half of
-// q_abs (2 x 8 KB), the peer's partial scores (2 x 16 KB), P (2 x 16 KB).
+// q_abs (2 x 8 KB), peer partial scores (2 x 16 KB), P (2 x 16 KB).
 //
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..5 = softmax
-// and epilogue, one thread per head row (TMEM lane). The softmax runs one
-// page behind the score MMAs so the partial-score exchange overlaps the next
-// page's MMAs.
+// and epilogue, one thread per head row (TMEM lane). The score MMAs run two
+// pages ahead of the value MMAs; the softmax of page g-1 is interleaved with
+// the reads of page g so every exchange's latency is covered by other work.
 #include <cudaTypedefs.h>
 
 #include "mla_internal.cuh"
@@ -46,32 +51,37 @@ constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16,
 constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
 constexpr uint32_t kQkrBytes = 128 * 64;    // [128 heads][32] bf16, 64B swizzle
-constexpr uint32_t kXBytes = 8 * 128 * 16;  // peer partial scores: [8][128 heads] x 16 B (fp16)
-constexpr uint32_t kPBytes = 128 * 128;     // P [128 heads][64 tokens] bf16, 128B swizzle
+constexpr uint32_t kXBytes = 8 * 128 * 16;  // peer partial scores: [8 groups of 4 tokens][128 heads] fp32
+constexpr uint32_t kPBytes = 128 * 128;     // P [128 heads][64 tokens] bf16, 128B swizzle, K-major
+constexpr uint32_t kPHalfBytes = kPBytes / 2;
+constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
 
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQkr = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;
 constexpr uint32_t kOffP = kOffX + 2 * kXBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffMX = kOffP + 2 * kPBytes;   // peer page maxima [2][128]
+constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;  // peer softmax sums [2][128]
+constexpr uint32_t kOffBar = kOffLX + 2 * kVecBytes;
 
 // barrier indices
 enum {
   FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
   SF0 = QCF + 1, SFREE0 = SF0 + 2, PF0 = SFREE0 + 2, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE0 = XF0 + 2,
-  OFREE = XE0 + 2, MMAD = OFREE + 1, kNumBars = MMAD + 1
+  MXF0 = XE0 + 2, LXF0 = MXF0 + 2, OFREE = LXF0 + 2, MMAD = OFREE + 1, kNumBars = MMAD + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffSlots + 16 + 1024;  // + alignment slack
+constexpr uint32_t kSmemBytes = kOffSlots + 16;  // the base is checked to be 1024-byte aligned
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384, kTmCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 
 struct TileInfo {
-  int g;       // CTA-local tile counter
+  int g;       // CTA-local page counter
   int item;    // partial index
-  int li;      // item counter within this worker
+  int li;      // range counter within this worker
   int first, last;
   int tok0;    // first token of the page
   int n_att;   // tokens this query attends
@@ -82,9 +92,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
                  const __grid_constant__ CUtensorMap map_qkr, const uint16_t* __restrict__ q_abs,
                  const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, float sl2,
                  Plan plan, int32_t* err_word) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report_error(err_word, MLA_ERR_CUDA);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int worker = blockIdx.x >> 1, j = blockIdx.y;
@@ -102,19 +115,24 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_init(bar(QKRE0 + i), 1);
       mbar_init(bar(SF0 + i), 1);
       mbar_init(bar(SFREE0 + i), 128);
-      mbar_init(bar(PF0 + i), 128);
-      mbar_init(bar(PVD0 + i), 1);
-      mbar_init(bar(XF0 + i), 1);   // armed by this CTA, filled by the peer's st.async
-      mbar_init(bar(XE0 + i), 4);   // one arrive per softmax warp of the peer
+      mbar_init(bar(PF0 + i), 129);  // 128 local halves + the arming arrive for the peer's half
+      mbar_init(bar(PVD0 + i), 2);   // the value MMAs of this page done in both CTAs
+      mbar_init(bar(XF0 + i), 1);    // armed here, filled by the peer's st.async
+      mbar_init(bar(XE0 + i), 4);    // one arrive per softmax warp of the peer
+      mbar_init(bar(MXF0 + i), 1);
+      mbar_init(bar(LXF0 + i), 1);
     }
     mbar_init(bar(QCF), 128);
     mbar_init(bar(OFREE), 128);
     mbar_init(bar(MMAD), 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // expect the peer's partial scores of this CTA's first two pages
-    mbar_arrive_expect_tx(bar(XF0), kXBytes);
-    mbar_arrive_expect_tx(bar(XF0 + 1), kXBytes);
+    for (int i = 0; i < 2; ++i) {
+      mbar_arrive_expect_tx(bar(XF0 + i), kXBytes);
+      mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
+      mbar_arrive_expect_tx(bar(MXF0 + i), kVecBytes);
+      mbar_arrive_expect_tx(bar(LXF0 + i), kVecBytes);
+    }
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_c);
@@ -195,20 +213,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, 256, false, true);
-      // descriptor templates (start address added per use, in 16-byte units)
+      // descriptor templates; the start address is added per use
       const uint64_t dQK_c = smem_desc(0, 16, 1024, kSwizzle128B);
       const uint64_t dQK_r = smem_desc(0, 16, 512, kSwizzle64B);
       const uint64_t dPV_a = smem_desc(0, 16, 1024, kSwizzle128B);
       const uint64_t dPV_b = smem_desc(0, kCBoxBytes, 1024, kSwizzle128B);
-      // start-address field of a descriptor: 14 bits of (shared address >> 4);
-      // shared addresses can carry high bits that must not spill into the
-      // neighbouring fields
+      // start-address field: 14 bits of (shared address >> 4). Shared
+      // addresses of the second CTA of a cluster carry high bits that must
+      // not spill into the neighbouring descriptor fields.
       auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };
       int stage = 0;
       uint32_t ph = 0;
       int g = 0;
       bool ok = true;
-      // pending value MMAs: (tile, stage, first-of-range, range counter)
+      // pending value MMAs: (page, stage, first-of-range, range counter)
       int pq_t[3], pq_s[3], pq_f[3], pq_l[3];
       int pq_head = 0, pq_n = 0;
 
@@ -216,13 +234,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         const int pb = t & 1;
         if (!wait_phase(bar(PF0 + pb), (t >> 1) & 1, abort_flag, err_word)) return false;
         if (first && li > 0 && !wait_phase(bar(OFREE), (li - 1) & 1, abort_flag, err_word)) return false;
+        // arm the P buffer for page t+2; its peer half can only come after this
+        // page's value MMAs (waited through PVD by the peer)
+        mbar_arrive_expect_tx(bar(PF0 + pb), kPHalfBytes);
+        fence_proxy_async_smem();  // P written by generic stores, read by the tensor core
         tc_fence_after();
         const uint64_t ad = dPV_a + da(sbase + kOffP + pb * kPBytes);
         const uint64_t bd = dPV_b + da(sbase + kOffStage + st * kStageBytes);
         mma_ss(tmem + kTmO, ad, bd, kIdPV, first ? 0u : 1u);
 #pragma unroll
         for (int ks = 1; ks < 4; ++ks) mma_ss(tmem + kTmO, ad + (ks * 32 >> 4), bd + (ks * 2048 >> 4), kIdPV, 1u);
-        mma_commit(bar(PVD0 + pb));
+        mma_commit_multicast(bar(PVD0 + pb), 0x3);
         mma_commit(bar(EMPTY0 + st));
         return true;
       };
@@ -276,10 +298,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const int row = quad * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO, tQ = tmem + lane_off + kTmQ;
-    const uint32_t x_local = sbase + kOffX;
-    const uint32_t x_remote = mapa(x_local, peer);
-    const uint32_t xf_remote0 = mapa(bar(XF0), peer), xe_remote0 = mapa(bar(XE0), peer);
     const int tid128 = threadIdx.x - 64;
+    // remote (peer) addresses: its buffers and barriers at the same offsets
+    const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
+    const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
+    const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE0), peer), r_pf = mapa(bar(PF0), peer);
+    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF0), peer);
+    // P chunk (8 tokens = 16 bytes) c of this row, 128B swizzle
+    const uint32_t prow_off = (uint32_t)row * 128;
+    auto pchunk = [&](int c) -> uint32_t { return prow_off + (uint32_t)((c ^ (row & 7)) * 16); };
 
     auto load_qc = [&](int it) {
       const int b = plan.item_seq[it];
@@ -300,50 +327,64 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_arrive(bar(QCF));
     };
 
-    float s_prev[64];
+    float s_keep[32];  // this CTA's partial scores of its own 32 tokens, page g
+    float x[32];       // full scores (log2 units) of its own tokens, page g-1
+    float mt_mine = -INFINITY;
     TileInfo pv{};
     bool have_prev = false, ok = true;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_ref = -INFINITY, l_mine = 0.f;
 
-    // Finish page t: merge the peer's partial, online softmax, P to shared
-    // memory, and for the last page of a range the normalised output.
-    auto finish = [&](const TileInfo& t) -> bool {
+    // B1(t): add the peer's partial for this CTA's tokens, mask, page maximum,
+    // and send that maximum to the peer.
+    auto stage_b1 = [&](const TileInfo& t) -> bool {
       const int xb = t.g & 1;
       if (!wait_phase(bar(XF0 + xb), (t.g >> 1) & 1, abort_flag, err_word)) return false;
       if (tid128 == 0) mbar_arrive_expect_tx(bar(XF0 + xb), kXBytes);  // arm for page t+2
-      const uint32_t xa = x_local + xb * kXBytes + (uint32_t)row * 16;
+      const uint32_t xa = sbase + kOffX + xb * kXBytes + (uint32_t)row * 16;
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) {
-        uint4 w;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(xa + q8 * 128 * 16));
-        const float2 a = f16x2_to_f32(w.x), b2 = f16x2_to_f32(w.y), c2 = f16x2_to_f32(w.z), d2 = f16x2_to_f32(w.w);
-        s_prev[8 * q8 + 0] += a.x; s_prev[8 * q8 + 1] += a.y;
-        s_prev[8 * q8 + 2] += b2.x; s_prev[8 * q8 + 3] += b2.y;
-        s_prev[8 * q8 + 4] += c2.x; s_prev[8 * q8 + 5] += c2.y;
-        s_prev[8 * q8 + 6] += d2.x; s_prev[8 * q8 + 7] += d2.y;
+        float4 w;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(w.x), "=f"(w.y), "=f"(w.z), "=f"(w.w) : "r"(xa + q8 * 128 * 16));
+        x[4 * q8 + 0] = (x[4 * q8 + 0] + w.x) * sl2;
+        x[4 * q8 + 1] = (x[4 * q8 + 1] + w.y) * sl2;
+        x[4 * q8 + 2] = (x[4 * q8 + 2] + w.z) * sl2;
+        x[4 * q8 + 3] = (x[4 * q8 + 3] + w.w) * sl2;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xe_remote0 + 8u * xb);
-      // mask tokens past this query's causal limit (only on the last pages)
-      const int nv = t.n_att - t.tok0;
-      if (nv < 64) {
+      if (lane == 0) mbar_arrive_remote(r_xe + 8u * xb);
+      const int nv = t.n_att - (t.tok0 + 32 * (int)rank);  // valid tokens among this CTA's 32
+      if (nv < 32) {
 #pragma unroll
-        for (int jj = 0; jj < 64; ++jj)
-          if (jj >= nv) s_prev[jj] = -INFINITY;
+        for (int jj = 0; jj < 32; ++jj)
+          if (jj >= nv) x[jj] = -INFINITY;
       }
-      float mt = s_prev[0];
+      float m = x[0];
 #pragma unroll
-      for (int jj = 1; jj < 64; ++jj) mt = fmaxf(mt, s_prev[jj]);
+      for (int jj = 1; jj < 32; ++jj) m = fmaxf(m, x[jj]);
+      mt_mine = m;
+      st_async_b32(r_mx + xb * kVecBytes + (uint32_t)row * 4, __float_as_uint(m), r_mxf + 8u * xb);
+      return true;
+    };
+
+    // B2(t): common page maximum, online-softmax update, this CTA's half of P
+    // (to both CTAs), and for the last page of a range the normalised output.
+    auto stage_b2 = [&](const TileInfo& t) -> bool {
+      const int xb = t.g & 1;
+      if (!wait_phase(bar(MXF0 + xb), (t.g >> 1) & 1, abort_flag, err_word)) return false;
+      if (tid128 == 0) mbar_arrive_expect_tx(bar(MXF0 + xb), kVecBytes);  // arm for page t+2
+      float m_peer;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_peer) : "r"(sbase + kOffMX + xb * kVecBytes + (uint32_t)row * 4));
+      const float mt = fmaxf(mt_mine, m_peer);  // identical in both CTAs
       bool need = false;
       float alpha = 1.f;
       if (t.first) {
-        m_run = mt;
-        l_run = 0.f;
-      } else if (mt > m_run + kRescaleThreshold) {
-        alpha = ex2(m_run - mt);
-        l_run *= alpha;
-        m_run = mt;
+        m_ref = mt;
+        l_mine = 0.f;
+      } else if (mt > m_ref + kRescaleThreshold) {
+        alpha = ex2(m_ref - mt);
+        l_mine *= alpha;
+        m_ref = mt;
         need = true;
       }
       if (__any_sync(0xffffffffu, need)) {
@@ -361,34 +402,44 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         }
         tmem_wait_st();
       }
-      // the P buffer of page t-2 must have been consumed
+      // both CTAs' value MMAs of page t-2 have consumed this P buffer
       if (t.g >= 2 && !wait_phase(bar(PVD0 + xb), ((t.g >> 1) & 1) ^ 1, abort_flag, err_word)) return false;
-      const float mref = m_run == -INFINITY ? 0.f : m_run;  // all-masked page: every p is 0
+      const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // all-masked so far: every p is 0
+      const uint32_t pl = sbase + kOffP + xb * kPBytes, pr = r_p + xb * kPBytes;
+      const uint32_t pfr = r_pf + 8u * xb;
       float lsum = 0.f;
-      const uint32_t prow = sbase + kOffP + xb * kPBytes + (uint32_t)row * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t pw[4];
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        uint32_t* pw = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const float p0 = ex2(s_prev[8 * c + 2 * v] - mref);
-          const float p1 = ex2(s_prev[8 * c + 2 * v + 1] - mref);
+          const float p0 = ex2(x[8 * c + 2 * v] - mref);
+          const float p1 = ex2(x[8 * c + 2 * v + 1] - mref);
           pw[v] = cvt_bf16x2(p0, p1);
           lsum += bf16_lo(pw[v]) + bf16_hi(pw[v]);
         }
-        const uint32_t a = prow + (uint32_t)((c ^ (row & 7)) * 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pw[0]), "r"(pw[1]), "r"(pw[2]),
-                     "r"(pw[3])
+        const uint32_t off = pchunk(4 * (int)rank + c);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pl + off), "r"(w.x), "r"(w.y), "r"(w.z),
+                     "r"(w.w)
                      : "memory");
+        st_async_v4(pr + off, w, pfr);
       }
-      l_run += lsum;
-      fence_proxy_async_smem();
+      l_mine += lsum;
       tc_fence_before();
       mbar_arrive(bar(PF0 + xb));
       if (t.last) {
+        // softmax sum over both token halves, then the normalised output
+        const int lb = t.li & 1;
+        st_async_b32(r_lx + lb * kVecBytes + (uint32_t)row * 4, __float_as_uint(l_mine), r_lxf + 8u * lb);
+        if (!wait_phase(bar(LXF0 + lb), (t.li >> 1) & 1, abort_flag, err_word)) return false;
+        if (tid128 == 0) mbar_arrive_expect_tx(bar(LXF0 + lb), kVecBytes);  // arm for range li+2
+        float l_peer;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l_peer) : "r"(sbase + kOffLX + lb * kVecBytes + (uint32_t)row * 4));
+        const float l_tot = rank == 0 ? l_mine + l_peer : l_peer + l_mine;
         if (!wait_phase(bar(PVD0 + xb), (t.g >> 1) & 1, abort_flag, err_word)) return false;
         tc_fence_after();
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
         const size_t orow = ((size_t)t.item * n_q + j) * H + row;
         float4* dst = reinterpret_cast<float4*>(plan.o_part + orow * kDC + 256 * rank);
 #pragma unroll 1
@@ -406,7 +457,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         tc_fence_before();
         mbar_arrive(bar(OFREE));
         if (rank == 0 && row < H)
-          plan.lse_part[orow] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+          plan.lse_part[orow] = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
       }
       return true;
     };
@@ -422,20 +473,30 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       const int ntiles = pg1 - pg0;
       for (int i = 0; i < ntiles; ++i, ++g) {
         const int sb = g & 1;
-        // this CTA's partial scores of page g (its 288 columns), pre-scaled to log2 units
+        // B1 of the previous page needs only the peer, not this page's scores
+        if (have_prev) {
+#pragma unroll
+          for (int v = 0; v < 32; ++v) x[v] = s_keep[v];
+          if (!stage_b1(pv)) { ok = false; break; }
+        }
+        // A: this CTA's partial scores of page g (its 288 columns)
         if (!wait_phase(bar(SF0 + sb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
         tc_fence_after();
-        float s_cur[64];
         {
           uint32_t r[32];
-          tmem_ld32(tS + 64 * sb, r);
+          // the other CTA's tokens first: send them
+          tmem_ld32(tS + 64 * sb + 32 * peer, r);
+          tmem_wait_ld();
+          if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word, true)) { ok = false; break; }
+          const uint32_t xa = r_x + sb * kXBytes + (uint32_t)row * 16;
+          const uint32_t xf = r_xf + 8u * sb;
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8)
+            st_async_v4(xa + q8 * 128 * 16, make_uint4(r[4 * q8], r[4 * q8 + 1], r[4 * q8 + 2], r[4 * q8 + 3]), xf);
+          tmem_ld32(tS + 64 * sb + 32 * rank, r);
           tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 32; ++v) s_cur[v] = __uint_as_float(r[v]) * sl2;
-          tmem_ld32(tS + 64 * sb + 32, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int v = 0; v < 32; ++v) s_cur[32 + v] = __uint_as_float(r[v]) * sl2;
+          for (int v = 0; v < 32; ++v) s_keep[v] = __uint_as_float(r[v]);
         }
         tc_fence_before();
         mbar_arrive(bar(SFREE0 + sb));
@@ -454,32 +515,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           }
           fence_proxy_async_smem();
         }
-        // send the partial to the peer (fp16 pairs), completing its barrier
-        if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word, true)) { ok = false; break; }
-        {
-          const uint32_t xa = x_remote + sb * kXBytes + (uint32_t)row * 16;
-          const uint32_t xf = xf_remote0 + 8u * sb;
-#pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            uint4 w;
-            w.x = cvt_f16x2(s_cur[8 * q8 + 0], s_cur[8 * q8 + 1]);
-            w.y = cvt_f16x2(s_cur[8 * q8 + 2], s_cur[8 * q8 + 3]);
-            w.z = cvt_f16x2(s_cur[8 * q8 + 4], s_cur[8 * q8 + 5]);
-            w.w = cvt_f16x2(s_cur[8 * q8 + 6], s_cur[8 * q8 + 7]);
-            st_async_v4(xa + q8 * 128 * 16, w, xf);
-          }
-        }
         // every score MMA of this range is done: stage the next range's query
         if (i == ntiles - 1 && it + 1 < it1) load_qc(it + 1);
-        if (have_prev && !finish(pv)) { ok = false; break; }
+        if (have_prev && !stage_b2(pv)) { ok = false; break; }
         pv = TileInfo{g, it, li, i == 0, i == ntiles - 1, tok0, n_att};
-#pragma unroll
-        for (int v = 0; v < 64; ++v) s_prev[v] = s_cur[v];
         have_prev = true;
         if (++stage == kStages) stage = 0;
       }
     }
-    if (ok && have_prev) finish(pv);
+    if (ok && have_prev) {
+#pragma unroll
+      for (int v = 0; v < 32; ++v) x[v] = s_keep[v];
+      ok = stage_b1(pv) && stage_b2(pv);
+    }
   }
 
   // ------------------------------------------------------------ teardown

@@ -252,3 +252,23 @@ __device__ __forceinline__ float2 f16x2_to_f32(uint32_t w) {
 }
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+// Arrive on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` once every tcgen05 operation this thread issued so far completes.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// Asynchronous 4-byte store into another CTA's shared memory with complete_tx.
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+}  // namespace sm100
+}  // namespace mla
