@@ -64,7 +64,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -209,31 +209,44 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step():
         q_abs = mla.absorb_q(q_nope, q_rope, w_uk, bufs["q_abs"])
-        if ev is not None:
-            ev[1].record(stream)
         mla.decode_paged(q_abs, cache, bt, sl, n_q=n_q, num_splits=G, workspace=bufs["workspace"],
                          err_word=err)
-        if ev is not None:
-            ev[2].record(stream)
         mla.combine(bufs["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=bufs["u"], lse=bufs["lse"])
-        if ev is not None:
-            ev[3].record(stream)
         mla.out_proj(bufs["u"], w_uv, bufs["out"])
-        if ev is not None:
-            ev[4].record(stream)
 
+    # eager warm-up (compiles nothing; checks the error word), then one CUDA graph
+    # holding the whole step so the timed region measures device time only
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    graph = capture(step)
+    # one graph per call, for the per-kernel phase times
+    sub = [
+        capture(lambda: mla.absorb_q(q_nope, q_rope, w_uk, bufs["q_abs"])),
+        capture(lambda: mla.decode_paged(bufs["q_abs"], cache, bt, sl, n_q=n_q, num_splits=G,
+                                         workspace=bufs["workspace"], err_word=err)),
+        capture(lambda: mla.combine(bufs["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=bufs["u"],
+                                    lse=bufs["lse"])),
+        capture(lambda: mla.out_proj(bufs["u"], w_uv, bufs["out"])),
+    ]
+    for _ in range(args.warmup):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+
+    t_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -243,15 +256,15 @@ def run_ours(args):
     wall0 = time.perf_counter()
     for k in range(args.steps):
         flush.zero_()
-        step(events[k])
+        t_start[k].record(stream)
+        graph.replay()
+        t_end[k].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    phase = np.array([[events[k][i].elapsed_time(events[k][i + 1]) for i in range(4)]
-                      for k in range(args.steps)])  # ms: absorb, decode, combine, out_proj
-    step_ms = phase.sum(axis=1)
+    step_ms = np.array([t_start[k].elapsed_time(t_end[k]) for k in range(args.steps)])
     total_ms = float(step_ms.sum())
     if dist is not None:
         t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
@@ -259,6 +272,20 @@ def run_ours(args):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = ws_ * T * args.steps / (total_ms * 1e-3)
+    # per-kernel phase times: the four calls replayed as separate graphs behind a
+    # short device-side sleep, so every launch is queued before the first event
+    n_phase = min(args.steps, 200)
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    phase = np.zeros((n_phase, 4))
+    for k in range(n_phase):
+        flush.zero_()
+        torch.cuda._sleep(200000)
+        pev[0].record(stream)
+        for i in range(4):
+            sub[i].replay()
+            pev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        phase[k] = [pev[i].elapsed_time(pev[i + 1]) for i in range(4)]
 
     # ---------------------------------------------------------------- end to end
     # Per step: the new queries, block table and context lengths go host->device
@@ -334,6 +361,7 @@ def run_ours(args):
                          "tensor_peak_tflops": tflops},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 5 * args.steps,
+            "timing": "CUDA-graph replay of the whole step; events on the launching stream",
             "clocks": clk,
             "wall_s_timed_region": wall,
         }
@@ -358,7 +386,7 @@ def mla_kernel_rev():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

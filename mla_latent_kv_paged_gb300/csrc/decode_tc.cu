@@ -35,8 +35,6 @@
 // and epilogue, one thread per head row (TMEM lane). The score MMAs run two
 // pages ahead of the value MMAs; the softmax of page g-1 is interleaved with
 // the reads of page g so every exchange's latency is covered by other work.
-#include <cudaTypedefs.h>
-
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -62,7 +60,8 @@ constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;
 constexpr uint32_t kOffP = kOffX + 2 * kXBytes;
 constexpr uint32_t kOffMX = kOffP + 2 * kPBytes;   // peer page maxima [2][128]
 constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;  // peer softmax sums [2][128]
-constexpr uint32_t kOffBar = kOffLX + 2 * kVecBytes;
+constexpr uint32_t kOffTok = kOffLX + 2 * kVecBytes;  // "partial consumed" tokens from the peer [2][4]
+constexpr uint32_t kOffBar = kOffTok + 2 * 4 * 4;
 
 // barrier indices
 enum {
@@ -118,7 +117,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_init(bar(PF0 + i), 129);  // 128 local halves + the arming arrive for the peer's half
       mbar_init(bar(PVD0 + i), 2);   // the value MMAs of this page done in both CTAs
       mbar_init(bar(XF0 + i), 1);    // armed here, filled by the peer's st.async
-      mbar_init(bar(XE0 + i), 4);    // one arrive per softmax warp of the peer
+      mbar_init(bar(XE0 + i), 1);    // armed here, completed by the peer's four 4-byte tokens
       mbar_init(bar(MXF0 + i), 1);
       mbar_init(bar(LXF0 + i), 1);
     }
@@ -132,6 +131,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
       mbar_arrive_expect_tx(bar(MXF0 + i), kVecBytes);
       mbar_arrive_expect_tx(bar(LXF0 + i), kVecBytes);
+      mbar_arrive_expect_tx(bar(XE0 + i), 16);
     }
   }
   if (warp == 0 && lane == 0) {
@@ -303,6 +303,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
     const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
     const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE0), peer), r_pf = mapa(bar(PF0), peer);
+    const uint32_t r_tok = mapa(sbase + kOffTok, peer);
     const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF0), peer);
     // P chunk (8 tokens = 16 bytes) c of this row, 128B swizzle
     const uint32_t prow_off = (uint32_t)row * 128;
@@ -352,7 +353,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         x[4 * q8 + 3] = (x[4 * q8 + 3] + w.w) * sl2;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(r_xe + 8u * xb);
+      // tell the peer this warp has read its partial (a 4-byte token completes
+      // the peer's barrier; the loads above have all returned by now)
+      if (lane == 0) st_async_b32(r_tok + (uint32_t)(xb * 4 + quad) * 4, 1u, r_xe + 8u * xb);
       const int nv = t.n_att - (t.tok0 + 32 * (int)rank);  // valid tokens among this CTA's 32
       if (nv < 32) {
 #pragma unroll
@@ -487,7 +490,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           // the other CTA's tokens first: send them
           tmem_ld32(tS + 64 * sb + 32 * peer, r);
           tmem_wait_ld();
-          if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word, true)) { ok = false; break; }
+          if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
+          if (g >= 2 && tid128 == 0) mbar_arrive_expect_tx(bar(XE0 + sb), 16);  // arm for page g+2
           const uint32_t xa = r_x + sb * kXBytes + (uint32_t)row * 16;
           const uint32_t xf = r_xf + 8u * sb;
 #pragma unroll
@@ -546,35 +550,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
   }
 }
 
-// ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
+// ---------------------------------------------------------------- host side
 int decode_max_workers() {
   static bool attr_set = false;
   if (!attr_set) {
@@ -606,11 +584,13 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
                           int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s) {
   CUtensorMap map_c, map_kr, map_qkr;
-  const uint64_t cache_rows = (uint64_t)num_pages * kPage;
-  const uint64_t q_rows = (uint64_t)B * n_q * H;
-  if (!make_map(&map_c, cache, kRow, cache_rows, kRow * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&map_kr, cache, kRow, cache_rows, kRow * 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_map(&map_qkr, q_abs, kRow, q_rows, kRow * 2, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+  const uint64_t q_dims[2] = {kRow, (uint64_t)B * n_q * H};
+  const uint64_t row_stride[1] = {kRow * 2};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 128};
+  if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
+      !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64) ||
+      !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of the library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -84,6 +85,12 @@ __device__ inline uint16_t float_to_bf16(float f) {
 __device__ inline uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)float_to_bf16(lo) | ((uint32_t)float_to_bf16(hi) << 16);
 }
+
+// ---------------------------------------------------------------- tensor maps
+// bf16 tensor map of `rank` dims (dims[0] innermost), byte strides of dims
+// 1..rank-1, box extents, swizzle span in bytes (0, 32, 64 or 128).
+bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box, int swizzle_bytes);
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
