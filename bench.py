@@ -335,15 +335,7 @@ def run_ours(args):
         dec_ms = float(phase[:, 1].mean())
         dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
         achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
-        traffic = None
-        tpath = os.path.join(ROOT, "profiles", "decode_traffic.json")
-        if os.path.exists(tpath):
-            try:
-                tj = json.load(open(tpath))
-                if tj.get("kernel_rev") == mla_kernel_rev():
-                    traffic = tj.get("bytes_per_launch")
-            except Exception:
-                traffic = None
+        traffic = stored_traffic()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -370,6 +362,18 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def stored_traffic():
+    """dram bytes per decode launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "decode_tc_v3_b32_l4096.md")
+    try:
+        kv = dict(ln.split(":", 1) for ln in open(path) if ln.startswith(("traffic_bytes_per_launch:", "kernel_rev:")))
+        if kv.get("kernel_rev", "").strip() == mla_kernel_rev():
+            return int(kv["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
 
 
 def mla_kernel_rev():
