@@ -151,6 +151,34 @@ mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_spl
                        uint16_t* u, float* lse, void* stream);
 
 /* ------------------------------------------------------------------------
+ * mla_decode_noalloc — mla_decode_paged followed by mla_combine for callers
+ * that cannot provide a workspace. No page has a counterpart: this is a
+ * deployment convenience of this library, not a step of the method.
+ *
+ * Who needs it: a serving loop that reserves all device memory for its KV
+ * cache at start-up and never allocates afterwards (a cudaMalloc in the step
+ * can block on the device and stall every request in flight), or a caller
+ * that reaches the GPU through an interface exposing only its own tensors.
+ * The plan and partial results live instead in one fixed device array of
+ * mla_decode_noalloc_max_bytes() bytes (32 MiB) inside the library, which
+ * every device that loads the library holds until the process exits. Calls
+ * whose plan and partials would not fit (see mla_decode_workspace_bytes)
+ * return MLA_ERR_WORKSPACE_TOO_SMALL without launching.
+ *
+ * The first call made with a device current looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture. All calls share the array: calls whose kernels overlap on the
+ * GPU (other streams, other host threads) race on it. Arguments and results
+ * are those of mla_decode_paged and mla_combine (u [B][n_q][H][512] bf16,
+ * lse [B][n_q][H] float or NULL). Nothing is allocated or freed. */
+size_t mla_decode_noalloc_max_bytes(void);
+mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              int B, int n_q, int H, int num_pages, int page_size,
+                              int max_pages_per_seq, float softmax_scale, int num_splits,
+                              uint16_t* u, float* lse, int32_t* err_word, void* stream);
+
+/* ------------------------------------------------------------------------
  * mla_out_proj — up-project the latent output through W_UV per head:
  *   out[t][h][v] = sum_c w_uv[h][v][c] * u[t][h][c]
  * Huny's Dev Blog section 3.2 (u_i W_i^UV after aggregation). fp32

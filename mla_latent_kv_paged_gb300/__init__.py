@@ -41,6 +41,7 @@ EXPORTS = [
     "mla_status_string", "mla_abi_version", "mla_cache_bytes_per_token", "mla_page_bytes",
     "mla_absorb_q", "mla_decode_default_splits", "mla_decode_workspace_bytes",
     "mla_decode_paged", "mla_combine", "mla_out_proj",
+    "mla_decode_noalloc_max_bytes", "mla_decode_noalloc",
 ]
 
 
@@ -87,6 +88,9 @@ def lib():
             L.mla_combine.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.mla_out_proj.restype = i
             L.mla_out_proj.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.mla_decode_noalloc_max_bytes.restype = sz
+            L.mla_decode_noalloc.restype = i
+            L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
             _lib = L
     return _lib
 
@@ -191,6 +195,31 @@ def combine(workspace, *, B: int, n_q: int, H: int, num_splits: int, u=None, lse
     st = lib().mla_combine(_ptr(workspace), B, n_q, H, num_splits, _ptr(_bits(u)), _ptr(lse),
                            _stream(stream))
     _check(st, "mla_combine")
+    return u, lse
+
+
+def decode_noalloc(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
+                   softmax_scale: float = DEFAULT_SCALE, u=None, lse=None, err_word=None, stream=None):
+    """decode_paged + combine with the scratch kept inside the library (no workspace).
+
+    For callers that must not allocate device memory during a step; see
+    ``mla_decode_noalloc`` in include/mla.h for the size limit and for the
+    rule that calls overlapping on the GPU race on the shared scratch.
+    """
+    import torch
+    B, max_pages = block_table.shape
+    H = q_abs.shape[-2]
+    if num_splits is None:
+        num_splits = default_splits(n_q)
+    dev = q_abs.device
+    if u is None:
+        u = torch.empty((B * n_q, H, D_C), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B * n_q, H), dtype=torch.float32, device=dev)
+    st = lib().mla_decode_noalloc(_ptr(_bits(q_abs)), _ptr(_bits(cache)), _ptr(block_table), _ptr(seq_lens),
+                                  B, n_q, H, cache.shape[0], cache.shape[1], max_pages, float(softmax_scale),
+                                  num_splits, _ptr(_bits(u)), _ptr(lse), _ptr(err_word), _stream(stream))
+    _check(st, "mla_decode_noalloc")
     return u, lse
 
 
