@@ -88,8 +88,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
                  const __grid_constant__ CUtensorMap map_qkr, const uint16_t* __restrict__ q_abs,
-                 const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, float sl2,
-                 Plan plan, int32_t* err_word) {
+                 const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, int num_pages,
+                 float sl2, Plan plan, int32_t* err_word) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -149,6 +149,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
   tc_fence_after();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
   const uint32_t tmem = *tmem_slot;
+  // set-up above overlaps the plan kernel; the plan and q_abs are read below
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int it0 = plan.range_item[worker], it1 = plan.range_item[worker + 1];
 
   if (warp == 0) {
@@ -205,6 +208,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         last_qph[qb] = (li >> 1) & 1;
       }
       const int pid = cur_next(ld);
+      // an id outside the pool loads zeros (TMA bounds) and is reported
+      if (lane == 0 && (pid < 0 || pid >= num_pages)) report_error(err_word, MLA_ERR_BOUNDS);
       if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
       if (lane == 0) {
         const uint32_t fb = bar(FULL0 + stage);
@@ -666,9 +671,8 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
   }
   const float sl2 = scale * 1.4426950408889634f;
   dim3 grid(2 * G, n_q, 1);
-  decode_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(map_c, map_kr, map_qkr, q_abs, block_table, n_q, H,
-                                                      max_pages, sl2, plan, err_word);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, q_abs,
+                    block_table, n_q, H, max_pages, num_pages, sl2, plan, err_word);
 }
 
 }  // namespace mla

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mla.h"
 
 namespace mla {
@@ -91,6 +93,27 @@ __device__ inline uint32_t pack_bf16x2(float lo, float hi) {
 // 1..rank-1, box extents, swizzle span in bytes (0, 32, 64 or 128).
 bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                const uint32_t* box, int swizzle_bytes);
+
+// ---------------------------------------------------------------- launch helper
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes; it must execute
+// griddepcontrol.wait before reading anything that kernel (or earlier work)
+// produced.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,

@@ -7,6 +7,7 @@
 // One block of 1024 threads. Integer work only; the output is a pure function
 // of (seq_lens, n_q, max_pages, G), so repeated calls give identical plans.
 #include "mla_internal.cuh"
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
@@ -156,16 +157,12 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     plan.range_item[p] = r;
   }
 
-  // 5. every page id that will be read must name a page of the pool
-  for (int g = tid; g < total; g += kPlanThreads) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (s_pstart[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    const int id = block_table[(size_t)lo * max_pages + (g - s_pstart[lo])];
-    if (id < 0 || id >= num_pages) report_error(err_word, MLA_ERR_BOUNDS);
-  }
+  // Page ids are checked by the decode kernel when it reads them. The plan
+  // does not read anything the previous kernel wrote, so it may run beside
+  // it; it waits for that kernel only before finishing, so the decode kernel
+  // that waits for the plan also sees everything written before it.
+  sm100::grid_launch_dependents();
+  sm100::grid_dependency_wait();
 }
 
 }  // namespace
@@ -179,9 +176,8 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  plan_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, block_table, B, n_q, max_pages, num_pages, G,
-                                            plan, err_word);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, block_table, B, n_q, max_pages,
+                    num_pages, G, plan, err_word);
 }
 
 }  // namespace mla

@@ -9,9 +9,11 @@
 //   The rotated positional query is copied to columns 512..575.
 // out_proj (section 3.2, u W^UV):
 //   D[v][t] = sum_c W_UV[h][v][c] u[t][h][c]            M = 128 value cols, N = rows t, K = 512
-//   A = W_UV[h] (K-major), B = u rows (K-major).
+//   A = W_UV[h] (K-major), B = u rows (K-major). Each 64-wide K slice has its
+//   own barrier, so the MMAs of a slice start as soon as it lands.
 // D sits in tensor memory with one lane per output column, so the epilogue
-// writes each output row t with 32 consecutive columns per warp.
+// writes each output row t with 32 consecutive columns per warp. N (rows per
+// tile) is 32, 64 or 128, the smallest that holds the batch's rows.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -23,37 +25,39 @@ using namespace sm100;
 constexpr int kThreads = 128;
 constexpr uint32_t kBoxRows = 128;  // A boxes: 128 rows x 64 bf16
 
-template <bool kAbsorb>
+template <bool kAbsorb, int kNT>
 struct ProjCfg {
-  static constexpr int NT = kAbsorb ? 128 : 64;        // rows t per tile (MMA N)
+  static constexpr int NT = kNT;                        // rows t per tile (MMA N)
   static constexpr int K = kAbsorb ? kDNope : kDC;      // reduction length
   static constexpr int KB = K / 64;                     // 64-wide K boxes
-  static constexpr uint32_t kABytes = kAbsorb ? 2 * kBoxRows * 128 : KB * kBoxRows * 128;
-  static constexpr uint32_t kBBytes = KB * NT * 128;
+  static constexpr uint32_t kABox = kBoxRows * 128;     // 16 KB
+  static constexpr uint32_t kBBox = NT * 128;
+  static constexpr uint32_t kABytes = kAbsorb ? 2 * kABox : KB * kABox;
+  static constexpr uint32_t kBBytes = KB * kBBox;
+  static constexpr int kBars = kAbsorb ? 1 : KB;        // load barriers
   static constexpr uint32_t kOffA = 0, kOffB = kABytes, kOffBar = kABytes + kBBytes;
-  static constexpr uint32_t kSmem = kOffBar + 64;
+  static constexpr uint32_t kSmem = kOffBar + 8 * (kBars + 1) + 16;
   static constexpr uint32_t kTmCols = NT < 32 ? 32 : NT;
 };
 
-template <bool kAbsorb>
+template <bool kAbsorb, int kNT>
 __global__ void __launch_bounds__(kThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const uint16_t* __restrict__ q_rope, uint16_t* __restrict__ out, int T, int H, int32_t* err_word) {
-  using C = ProjCfg<kAbsorb>;
+  using C = ProjCfg<kAbsorb, kNT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x, cblk = blockIdx.y;  // cblk: 128-column block of q_abs (absorb only)
-  const uint32_t bar_a = sbase + C::kOffBar, bar_b = bar_a + 8, bar_d = bar_a + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 24);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 28);
+  const uint32_t bar_ld = sbase + C::kOffBar, bar_d = bar_ld + 8 * C::kBars;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * (C::kBars + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffBar + 8 * (C::kBars + 1) + 4);
   if (sbase & 1023u) {
     if (threadIdx.x == 0) report_error(err_word, MLA_ERR_CUDA);
     return;
   }
   if (threadIdx.x == 0) {
-    mbar_init(bar_a, 1);
-    mbar_init(bar_b, 1);
+    for (int i = 0; i < C::kBars; ++i) mbar_init(bar_ld + 8 * i, 1);
     mbar_init(bar_d, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -68,19 +72,10 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above overlaps the previous kernel; its outputs are read below
+  grid_dependency_wait();
+  grid_launch_dependents();
 
-  if (threadIdx.x == 0) {
-    const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(bar_a, C::kABytes);
-    if (kAbsorb) {
-      // W_UK[h][i][c] as boxes of [128 i][64 c]: the two 64-column halves of this block
-      for (int m = 0; m < 2; ++m)
-        tma_load_3d(sbase + C::kOffA + m * kBoxRows * 128, &map_a, bar_a, cblk * 128 + m * 64, 0, h, pol);
-    } else {
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(sbase + C::kOffA + kb * kBoxRows * 128, &map_a, bar_a, kb * 64, 0, h, pol);
-    }
-  }
   // rotated positional query: copied unchanged next to the absorbed one
   if (kAbsorb && cblk == 0) {
     for (int i = threadIdx.x; i < T * (kDR / 8); i += kThreads) {
@@ -92,29 +87,45 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
   const uint32_t idesc = idesc_bf16(128, C::NT, kAbsorb, false);
   auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };
-  int phase = 0;
-  for (int t0 = 0; t0 < T; t0 += C::NT, phase ^= 1) {
+  const uint64_t bdesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffB);
+  uint32_t phase = 0;
+  for (int t0 = 0; t0 < T; t0 += C::NT, phase ^= 1u) {
     if (threadIdx.x == 0) {
-      mbar_arrive_expect_tx(bar_b, C::kBBytes);
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(sbase + C::kOffB + kb * C::NT * 128, &map_b, bar_b, kb * 64, h, t0, policy_evict_first());
-      bool ok = wait_phase(bar_a, 0, abort_flag, err_word) && wait_phase(bar_b, phase, abort_flag, err_word);
-      if (ok) {
-        tc_fence_after();
-        const uint64_t bdesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffB);
-        if (kAbsorb) {
+      const uint64_t pol = policy_evict_first();
+      bool ok = true;
+      if (kAbsorb) {
+        mbar_arrive_expect_tx(bar_ld, (t0 == 0 ? C::kABytes : 0) + C::kBBytes);
+        if (t0 == 0)  // W_UK[h][i][c] as boxes of [128 i][64 c]: the two 64-column halves of this block
+          for (int m = 0; m < 2; ++m)
+            tma_load_3d(sbase + C::kOffA + m * C::kABox, &map_a, bar_ld, cblk * 128 + m * 64, 0, h, pol);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(sbase + C::kOffB + kb * C::kBBox, &map_b, bar_ld, kb * 64, h, t0, pol);
+        ok = wait_phase(bar_ld, phase, abort_flag, err_word);
+        if (ok) {
+          tc_fence_after();
           // A is M-major: 64-column halves 16 KB apart (LBO), 8-row K groups 1 KB apart (SBO)
-          const uint64_t adesc = smem_desc(0, kBoxRows * 128, 1024, kSwizzle128B) + da(sbase + C::kOffA);
+          const uint64_t adesc = smem_desc(0, C::kABox, 1024, kSwizzle128B) + da(sbase + C::kOffA);
 #pragma unroll
           for (int ks = 0; ks < C::K / 16; ++ks)
-            mma_ss(tmem, adesc + (ks * 2048 >> 4), bdesc + (((ks >> 2) * C::NT * 128 + (ks & 3) * 32) >> 4), idesc,
+            mma_ss(tmem, adesc + (ks * 2048 >> 4), bdesc + (((ks >> 2) * C::kBBox + (ks & 3) * 32) >> 4), idesc,
                    ks > 0 ? 1u : 0u);
-        } else {
-          const uint64_t adesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffA);
+        }
+      } else {
+        for (int kb = 0; kb < C::KB; ++kb) {
+          const uint32_t b = bar_ld + 8 * kb;
+          mbar_arrive_expect_tx(b, (t0 == 0 ? C::kABox : 0) + C::kBBox);
+          if (t0 == 0) tma_load_3d(sbase + C::kOffA + kb * C::kABox, &map_a, b, kb * 64, 0, h, pol);
+          tma_load_3d(sbase + C::kOffB + kb * C::kBBox, &map_b, b, kb * 64, h, t0, pol);
+        }
+        const uint64_t adesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffA);
+        for (int kb = 0; kb < C::KB && ok; ++kb) {
+          ok = wait_phase(bar_ld + 8 * kb, phase, abort_flag, err_word);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < C::K / 16; ++ks)
-            mma_ss(tmem, adesc + (((ks >> 2) * kBoxRows * 128 + (ks & 3) * 32) >> 4),
-                   bdesc + (((ks >> 2) * C::NT * 128 + (ks & 3) * 32) >> 4), idesc, ks > 0 ? 1u : 0u);
+          for (int k4 = 0; k4 < 4; ++k4)
+            mma_ss(tmem, adesc + ((kb * C::kABox + k4 * 32) >> 4), bdesc + ((kb * C::kBBox + k4 * 32) >> 4), idesc,
+                   (kb > 0 || k4 > 0) ? 1u : 0u);
         }
       }
       mma_commit(bar_d);  // arrives once the MMAs (if any) finished
@@ -146,7 +157,6 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     __syncthreads();  // D and the B tile are free for the next rows
     tc_fence_after();
   }
-  // drain: the MMAs of the last tile completed before the epilogue read D
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -155,50 +165,49 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   }
 }
 
-template <bool kAbsorb>
-cudaError_t set_smem() {
+template <bool kAbsorb, int kNT>
+cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint16_t* q_rope, uint16_t* out,
+                        int T, int H, cudaStream_t s) {
+  using C = ProjCfg<kAbsorb, kNT>;
   static bool done = false;
   if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<kAbsorb>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)ProjCfg<kAbsorb>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<kAbsorb, kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmem);
     if (e != cudaSuccess) return e;
     done = true;
   }
-  return cudaSuccess;
+  const dim3 grid(H, kAbsorb ? kDC / 128 : 1);
+  return launch_pdl(proj_tc_kernel<kAbsorb, kNT>, grid, dim3(kThreads), C::kSmem, s, ma, mb, q_rope, out, T, H,
+                    (int32_t*)nullptr);
+}
+
+bool maps(CUtensorMap* ma, CUtensorMap* mb, const uint16_t* w, const uint16_t* act, int T, int H, int K, int nt) {
+  // weights [H][128][512]: boxes of 64 columns x 128 rows; activations [T][H][K]: 64 x 1 head x nt rows
+  const uint64_t da[3] = {kDC, 128, (uint64_t)H}, sa[2] = {kDC * 2, (uint64_t)128 * kDC * 2};
+  const uint64_t db[3] = {(uint64_t)K, (uint64_t)H, (uint64_t)T}, sb[2] = {(uint64_t)K * 2, (uint64_t)H * K * 2};
+  const uint32_t ba[3] = {64, kBoxRows, 1}, bb[3] = {64, 1, (uint32_t)nt};
+  return make_tmap(ma, w, 3, da, sa, ba, 128) && make_tmap(mb, act, 3, db, sb, bb, 128);
 }
 
 }  // namespace
 
 cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
                             uint16_t* q_abs, int T, int H, cudaStream_t s) {
-  using C = ProjCfg<true>;
+  const int nt = T <= 32 ? 32 : T <= 64 ? 64 : 128;
   CUtensorMap ma, mb;
-  // W_UK [H][128 i][512 c]: boxes of 64 c x 128 i; q_nope [T][H][128]: boxes of 64 i x 1 head x NT rows
-  const uint64_t da[3] = {kDC, kDNope, (uint64_t)H}, sa[2] = {kDC * 2, (uint64_t)kDNope * kDC * 2};
-  const uint64_t db[3] = {kDNope, (uint64_t)H, (uint64_t)T}, sb[2] = {kDNope * 2, (uint64_t)H * kDNope * 2};
-  const uint32_t ba[3] = {64, kBoxRows, 1}, bb[3] = {64, 1, (uint32_t)C::NT};
-  if (!make_tmap(&ma, w_uk, 3, da, sa, ba, 128) || !make_tmap(&mb, q_nope, 3, db, sb, bb, 128))
-    return cudaErrorInvalidValue;
-  cudaError_t e = set_smem<true>();
-  if (e != cudaSuccess) return e;
-  proj_tc_kernel<true><<<dim3(H, kDC / 128), kThreads, C::kSmem, s>>>(ma, mb, q_rope, q_abs, T, H, nullptr);
-  return cudaGetLastError();
+  if (!maps(&ma, &mb, w_uk, q_nope, T, H, kDNope, nt)) return cudaErrorInvalidValue;
+  if (nt == 32) return launch_proj<true, 32>(ma, mb, q_rope, q_abs, T, H, s);
+  if (nt == 64) return launch_proj<true, 64>(ma, mb, q_rope, q_abs, T, H, s);
+  return launch_proj<true, 128>(ma, mb, q_rope, q_abs, T, H, s);
 }
 
 cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
                             cudaStream_t s) {
-  using C = ProjCfg<false>;
+  const int nt = T <= 32 ? 32 : 64;
   CUtensorMap ma, mb;
-  // W_UV [H][128 v][512 c]: boxes of 64 c x 128 v; u [T][H][512]: boxes of 64 c x 1 head x NT rows
-  const uint64_t da[3] = {kDC, kDV, (uint64_t)H}, sa[2] = {kDC * 2, (uint64_t)kDV * kDC * 2};
-  const uint64_t db[3] = {kDC, (uint64_t)H, (uint64_t)T}, sb[2] = {kDC * 2, (uint64_t)H * kDC * 2};
-  const uint32_t ba[3] = {64, kBoxRows, 1}, bb[3] = {64, 1, (uint32_t)C::NT};
-  if (!make_tmap(&ma, w_uv, 3, da, sa, ba, 128) || !make_tmap(&mb, u, 3, db, sb, bb, 128))
-    return cudaErrorInvalidValue;
-  cudaError_t e = set_smem<false>();
-  if (e != cudaSuccess) return e;
-  proj_tc_kernel<false><<<dim3(H, 1), kThreads, C::kSmem, s>>>(ma, mb, nullptr, out, T, H, nullptr);
-  return cudaGetLastError();
+  if (!maps(&ma, &mb, w_uv, u, T, H, kDC, nt)) return cudaErrorInvalidValue;
+  if (nt == 32) return launch_proj<false, 32>(ma, mb, nullptr, out, T, H, s);
+  return launch_proj<false, 64>(ma, mb, nullptr, out, T, H, s);
 }
 
 }  // namespace mla

@@ -307,3 +307,14 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, u
 }
 }  // namespace sm100
 }  // namespace mla
+
+namespace mla {
+namespace sm100 {
+// Programmatic dependent launch: wait until the preceding kernel of the stream
+// has completed and its writes are visible; allow the next kernel to launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+}  // namespace sm100
+}  // namespace mla
