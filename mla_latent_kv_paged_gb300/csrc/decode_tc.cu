@@ -19,22 +19,26 @@
 // S_r[128 heads][64 tokens] (K = 288) with tcgen05 MMAs into tensor memory.
 // The softmax of a page is split by tokens: CTA r finishes tokens
 // [32r, 32r+32). It sends the partial scores of the other 32 tokens to the
-// peer (fp32, 16 KB, st.async into the peer's shared memory), adds the
+// peer (fp16 in log2 units, 8 KB, st.async into the peer's shared memory), adds the
 // peer's partial for its own tokens, and both CTAs exchange their page
 // maxima so they share one exact running maximum per head. Each CTA then
-// exponentiates its 32 tokens, writes its half of P[128][64] (bf16) into its
-// own and the peer's shared memory, and accumulates its 256-column half of
-// O[128][512] in tensor memory with the second MMA (P x C[64][256]).
+// exponentiates its 32 tokens into P (bf16): its own half goes to tensor
+// memory (the A operand of its value MMAs), a copy to the peer's shared
+// memory (the peer's A operand for those 16-token K steps). Each CTA
+// accumulates its 256-column half of O[128][512] in tensor memory with the
+// value MMAs (P x C[64][256]).
 //
-// Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S double
-// buffer [256,384), the CTA's latent half of q_abs as the MMA A operand
-// [384,512). Shared memory: 4-stage page ring (147 KB), the positional half of
-// q_abs (2 x 8 KB), peer partial scores (2 x 16 KB), P (2 x 16 KB).
+// Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S [256,320),
+// this CTA's P half for two pages [320,352), the CTA's latent half of q_abs as
+// the score MMAs' A operand [384,512). Shared memory: 5-stage page ring
+// (180 KB), the positional half of q_abs (2 x 8 KB), the peer's partial
+// scores (8 KB), the peer's P half (2 x 8 KB), the exchange vectors.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2..5 = softmax
-// and epilogue, one thread per head row (TMEM lane). The score MMAs run two
-// pages ahead of the value MMAs; the softmax of page g-1 is interleaved with
-// the reads of page g so every exchange's latency is covered by other work.
+// Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
+// value-MMA issuer, 3..6 = score readers (the peer's tokens of S, the query
+// stage-in), 7..14 = softmax and epilogue, two warps per TMEM lane quadrant
+// (one thread per head row, 16 tokens each). The score MMAs of page g+1 run
+// while the softmax of page g is in flight; the value MMAs trail by one page.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -43,44 +47,46 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kAWarps = 4;  // score readers: one per TMEM lane quadrant
 constexpr int kBWarps = 8;  // softmax: two per lane quadrant, 16 tokens each
 constexpr int kAThreads = kAWarps * 32, kBThreads = kBWarps * 32;
-constexpr int kThreads = 64 + kAThreads + kBThreads;
+constexpr int kThreads = 96 + kAThreads + kBThreads;
 constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16, 128B swizzle
 constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
 constexpr uint32_t kQkrBytes = 128 * 64;    // [128 heads][32] bf16, 64B swizzle
 constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of 8 tokens][128 heads] fp16
-constexpr uint32_t kPBytes = 128 * 128;     // P [128 heads][64 tokens] bf16, 128B swizzle, K-major
-constexpr uint32_t kPHalfBytes = kPBytes / 2;
+constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads][32 tokens] bf16, 64B swizzle
+constexpr uint32_t kPHalfBytes = kPPeerBytes;
 constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
 constexpr uint32_t kVec2Bytes = 2 * kVecBytes;  // one float per head and token quarter
 
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQkr = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;
-constexpr uint32_t kOffP = kOffX + 2 * kXBytes;
-constexpr uint32_t kOffMX = kOffP + 2 * kPBytes;      // peer page maxima [2][2 quarters][128]
+constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;   // peer partial scores (one page)
+constexpr uint32_t kOffP = kOffX + kXBytes;            // the peer's half of P, two pages
+constexpr uint32_t kOffMX = kOffP + 2 * kPPeerBytes;   // peer page maxima [2][2 quarters][128]
 constexpr uint32_t kOffMS = kOffMX + 2 * kVec2Bytes;   // this CTA's page maxima [2][2][128]
-constexpr uint32_t kOffLX = kOffMS + 2 * kVec2Bytes;   // peer softmax sums [2][2][128]
-constexpr uint32_t kOffLS = kOffLX + 2 * kVec2Bytes;   // this CTA's softmax sums [2][2][128]
-constexpr uint32_t kOffTok = kOffLS + 2 * kVec2Bytes;  // "partial consumed" tokens from the peer [2][8]
-constexpr uint32_t kOffBar = kOffTok + 2 * kBWarps * 4;
+constexpr uint32_t kOffLX = kOffMS + 2 * kVec2Bytes;   // peer softmax sums [2][128]
+constexpr uint32_t kOffLS = kOffLX + kVec2Bytes;       // this CTA's softmax sums [2][128]
+constexpr uint32_t kOffTok = kOffLS + kVec2Bytes;      // "partial consumed" tokens from the peer [8]
+constexpr uint32_t kOffBar = kOffTok + kBWarps * 4;
 
 // barrier indices
 enum {
   FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
-  SF0 = QCF + 1, SFREE0 = SF0 + 2, PF0 = SFREE0 + 2, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE0 = XF0 + 2,
-  MXF0 = XE0 + 2, LXF0 = MXF0 + 2, MSF0 = LXF0 + 2, LSF0 = MSF0 + 2, OFREE = LSF0 + 2, MMAD = OFREE + 1,
+  SF = QCF + 1, SFREE = SF + 1, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF = PVD0 + 2, XE = XF + 1,
+  MXF0 = XE + 1, LXF = MXF0 + 2, MSF0 = LXF + 1, LSF = MSF0 + 2, OFREE = LSF + 1, MMAD = OFREE + 1,
   kNumBars = MMAD + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffSlots + 16;  // the base is checked to be 1024-byte aligned
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmO = 0, kTmS = 256, kTmQ = 384, kTmCols = 512;
+// tensor memory columns: O[128][256] fp32, S[128][64] fp32, this CTA's half of P
+// (bf16 pairs) for two pages, the CTA's latent half of q_abs (bf16 pairs)
+constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384, kTmCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 
@@ -111,29 +117,29 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(QKRF0 + i), 1);
       mbar_init(bar(QKRE0 + i), 1);
-      mbar_init(bar(SF0 + i), 1);
-      mbar_init(bar(SFREE0 + i), kAThreads + kBThreads);
       mbar_init(bar(PF0 + i), kBThreads + 1);  // local quarters + the arming arrive for the peer's half
       mbar_init(bar(PVD0 + i), 2);   // the value MMAs of this page done in both CTAs
-      mbar_init(bar(XF0 + i), 1);    // armed here, filled by the peer's st.async
-      mbar_init(bar(XE0 + i), 1);    // armed here, completed by the peer's eight 4-byte tokens
       mbar_init(bar(MXF0 + i), 1);
-      mbar_init(bar(LXF0 + i), 1);
       mbar_init(bar(MSF0 + i), kBThreads);  // this CTA's page maxima written
-      mbar_init(bar(LSF0 + i), kBThreads);  // this CTA's softmax sums written
     }
+    mbar_init(bar(SF), 1);
+    mbar_init(bar(SFREE), kAThreads + kBThreads);
+    mbar_init(bar(XF), 1);   // armed here, filled by the peer's st.async
+    mbar_init(bar(XE), 1);   // armed here, completed by the peer's eight 4-byte tokens
+    mbar_init(bar(LXF), 1);
+    mbar_init(bar(LSF), kBThreads);  // this CTA's softmax sums written
     mbar_init(bar(QCF), kAThreads);
     mbar_init(bar(OFREE), kBThreads);
-    mbar_init(bar(MMAD), 1);
+    mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
     fence_mbar_init();
     for (int i = 0; i < 2; ++i) {
-      mbar_arrive_expect_tx(bar(XF0 + i), kXBytes);
       mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
       mbar_arrive_expect_tx(bar(MXF0 + i), kVec2Bytes);
-      mbar_arrive_expect_tx(bar(LXF0 + i), kVec2Bytes);
-      mbar_arrive_expect_tx(bar(XE0 + i), kBWarps * 4);
     }
+    mbar_arrive_expect_tx(bar(XF), kXBytes);
+    mbar_arrive_expect_tx(bar(XE), kBWarps * 4);
+    mbar_arrive_expect_tx(bar(LXF), kVec2Bytes);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_c);
@@ -238,104 +244,90 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Event driven: the value MMAs of a page are issued as soon as its P is
-    // ready, and the score MMAs of later pages whenever their tile has landed
-    // and a score buffer is free. Score MMAs are issued in two halves so a
-    // ready value MMA never waits behind a whole page of score MMAs.
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads feed the tensor pipe: warp 1 the score MMAs, warp 2 the value
+    // MMAs. An MMA issue stalls at the pipe's execution rate, so with one
+    // issuer the pipe idled whenever that thread waited for P or for a tile;
+    // with two, whichever has work ready keeps it busy. A value MMA of a page
+    // follows that page's score MMAs through S -> P, so its commit (EMPTY)
+    // also covers the page's score MMAs.
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(128, 256, false, true);
       // descriptor templates; the start address is added per use
       const uint64_t dQK_c = smem_desc(0, 16, 1024, kSwizzle128B);
       const uint64_t dQK_r = smem_desc(0, 16, 512, kSwizzle64B);
-      const uint64_t dPV_a = smem_desc(0, 16, 1024, kSwizzle128B);
+      const uint64_t dPV_a = smem_desc(0, 16, 512, kSwizzle64B);  // the peer's half of P
       const uint64_t dPV_b = smem_desc(0, kCBoxBytes, 1024, kSwizzle128B);
       // start-address field: 14 bits of (shared address >> 4). Shared
       // addresses of the second CTA of a cluster carry high bits that must
       // not spill into the neighbouring descriptor fields.
       auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };
-
-      // cursors over the pages of this worker: q = next score MMA, p = next value MMA
-      int q_it = it0, q_i = 0, q_g = 0, q_stage = 0, q_half = 0;
-      uint32_t q_ph = 0;
-      int p_it = it0, p_i = 0, p_g = 0, p_stage = 0;
       bool ok = true;
-      long long idle_since = clock64();
-      while (ok && p_it < it1) {
-        bool progress = false;
-        // ---- value MMAs of page p_g (A = P from shared memory, B = the page's latent half)
-        if (p_g < q_g) {
-          const int pb = p_g & 1, li = p_it - it0;
-          const bool first = (p_i == 0);
-          if (mbar_test(bar(PF0 + pb), (p_g >> 1) & 1) && (!first || li == 0 || mbar_test(bar(OFREE), (li - 1) & 1))) {
-            // arm the P buffer for page p_g+2; its peer half can only come after
-            // this page's value MMAs (waited through PVD by the peer)
-            mbar_arrive_expect_tx(bar(PF0 + pb), kPHalfBytes);
-            fence_proxy_async_smem();  // P written by generic stores, read by the tensor core
+      int g = 0, stage = 0;
+      uint32_t ph = 0;
+      if (warp == 1) {
+        // ---- score MMAs: S = q_abs half . [c ; k^R] half of the page
+        for (int it = it0; it < it1 && ok; ++it) {
+          const int li = it - it0, qb = li & 1;
+          const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+          // the range's query: latent half in tensor memory, positional half by TMA
+          if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word) ||
+              !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          for (int i = 0; i < ntiles; ++i, ++g) {
+            if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
+                !wait_phase(bar(SFREE), (g & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t ad = dPV_a + da(sbase + kOffP + pb * kPBytes);
-            const uint64_t bd = dPV_b + da(sbase + kOffStage + p_stage * kStageBytes);
-            mma_ss(tmem + kTmO, ad, bd, kIdPV, first ? 0u : 1u);
+            const uint32_t d = tmem + kTmS;
+            const uint64_t bc = dQK_c + da(sbase + kOffStage + stage * kStageBytes);
 #pragma unroll
-            for (int ks = 1; ks < 4; ++ks) mma_ss(tmem + kTmO, ad + (ks * 32 >> 4), bd + (ks * 2048 >> 4), kIdPV, 1u);
-            mma_commit_multicast(bar(PVD0 + pb), 0x3);
-            mma_commit(bar(EMPTY0 + p_stage));
-            ++p_g;
-            if (++p_stage == kStages) p_stage = 0;
-            if (++p_i == plan.item_page1[p_it] - plan.item_page0[p_it]) { p_i = 0; ++p_it; }
-            progress = true;
-          }
-        }
-        // ---- score MMAs of page q_g, in two halves
-        if (q_it < it1) {
-          const int li = q_it - it0, qb = li & 1, sb = q_g & 1;
-          const uint32_t d = tmem + kTmS + 64 * sb;
-          const uint64_t bc = dQK_c + da(sbase + kOffStage + q_stage * kStageBytes);
-          if (q_half == 0) {
-            const bool ready = (q_i != 0 || (mbar_test(bar(QCF), li & 1) && mbar_test(bar(QKRF0 + qb), (li >> 1) & 1))) &&
-                               mbar_test(bar(FULL0 + q_stage), q_ph) &&
-                               mbar_test(bar(SFREE0 + sb), ((q_g >> 1) & 1) ^ 1);
-            if (ready) {
-              tc_fence_after();
-              mma_ts(d, tmem + kTmQ, bc, kIdQK, 0u);
-#pragma unroll
-              for (int ks = 1; ks < 8; ++ks)
-                mma_ts(d, tmem + kTmQ + ks * 8, bc + (((ks >> 2) * kCBoxBytes + (ks & 3) * 32) >> 4), kIdQK, 1u);
-              q_half = 1;
-              progress = true;
-            }
-          } else {
-#pragma unroll
-            for (int ks = 8; ks < 16; ++ks)
-              mma_ts(d, tmem + kTmQ + ks * 8, bc + (((ks >> 2) * kCBoxBytes + (ks & 3) * 32) >> 4), kIdQK, 1u);
+            for (int ks = 0; ks < 16; ++ks)
+              mma_ts(d, tmem + kTmQ + ks * 8, bc + (((ks >> 2) * kCBoxBytes + (ks & 3) * 32) >> 4), kIdQK,
+                     ks > 0 ? 1u : 0u);
             const uint64_t ar = dQK_r + da(sbase + kOffQkr + qb * kQkrBytes);
-            const uint64_t br = dQK_r + da(sbase + kOffStage + q_stage * kStageBytes + 4 * kCBoxBytes);
+            const uint64_t br = dQK_r + da(sbase + kOffStage + stage * kStageBytes + 4 * kCBoxBytes);
             mma_ss(d, ar, br, kIdQK, 1u);
             mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
-            mma_commit(bar(SF0 + sb));
-            const int ntiles = plan.item_page1[q_it] - plan.item_page0[q_it];
-            if (q_i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
-            q_half = 0;
-            ++q_g;
-            if (++q_stage == kStages) { q_stage = 0; q_ph ^= 1u; }
-            if (++q_i == ntiles) { q_i = 0; ++q_it; }
-            progress = true;
+            mma_commit(bar(SF));
+            if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
+            if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
         }
-        if (progress) {
-          idle_since = clock64();
-        } else {
-          if (*abort_flag) { ok = false; break; }
-          __nanosleep(20);  // leave issue slots to the softmax warps sharing this scheduler
-          if (clock64() - idle_since > kWaitLimitCycles) {
-            *abort_flag = 1;
-            report_error(err_word, MLA_ERR_TIMEOUT);
-            ok = false;
+      } else {
+        // ---- value MMAs: O += P . C half, P from tensor memory (this CTA's
+        // tokens) and from shared memory (the peer's tokens)
+        for (int it = it0; it < it1 && ok; ++it) {
+          const int li = it - it0;
+          const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+          for (int i = 0; i < ntiles; ++i, ++g) {
+            const int pb = g & 1;
+            if (!wait_phase(bar(PF0 + pb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            // the first value MMA of a range overwrites O: the previous range's
+            // epilogue must have read it
+            if (i == 0 && li > 0 && !wait_phase(bar(OFREE), (li - 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            // arm the P buffer for page g+2; its peer half can only come after
+            // this page's value MMAs (waited through PVD by the peer)
+            mbar_arrive_expect_tx(bar(PF0 + pb), kPHalfBytes);
+            tc_fence_after();
+            const uint64_t ad = dPV_a + da(sbase + kOffP + pb * kPPeerBytes);
+            const uint64_t bd = dPV_b + da(sbase + kOffStage + stage * kStageBytes);
+            const uint32_t am = tmem + kTmP + 16 * pb;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+              if ((ks >> 1) == (int)rank)
+                mma_ts(tmem + kTmO, am + 8 * (ks & 1), bd + (ks * 2048 >> 4), kIdPV, acc);
+              else
+                mma_ss(tmem + kTmO, ad + ((ks & 1) * 32 >> 4), bd + (ks * 2048 >> 4), kIdPV, acc);
+            }
+            mma_commit_multicast(bar(PVD0 + pb), 0x3);
+            mma_commit(bar(EMPTY0 + stage));
+            if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
         }
       }
+      (void)ph;
       mma_commit(bar(MMAD));
     }
     __syncwarp();
@@ -347,16 +339,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO, tQ = tmem + lane_off + kTmQ;
     const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
     const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
-    const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE0), peer), r_pf = mapa(bar(PF0), peer);
-    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF0), peer);
+    const uint32_t r_xf = mapa(bar(XF), peer), r_xe = mapa(bar(XE), peer), r_pf = mapa(bar(PF0), peer);
+    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF), peer);
     const uint32_t r_tok = mapa(sbase + kOffTok, peer);
 
-    if (warp < 2 + kAWarps) {
+    if (warp < 3 + kAWarps) {
       // -------------------------------------------------------- A: score readers
       // Per page: read the peer's 32 tokens of this CTA's partial scores, send
       // them (log2 units, fp16) into the peer's shared memory, zero slack rows,
       // and stage the query of the next range.
-      const int atid = threadIdx.x - 64;  // 0 .. 127
+      const int atid = threadIdx.x - 96;  // 0 .. 127
       auto load_qc = [&](int it) {
         const int b = plan.item_seq[it];
         const size_t qrow = ((size_t)b * n_q + j) * H + row;
@@ -376,25 +368,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         mbar_arrive(bar(QCF));
       };
       if (it0 < it1) load_qc(it0);
-      int g = 0, stage = 0;
+      int g = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
-        const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
-        const int L = plan.seq_len_eff[b];
-        const int ntiles = pg1 - pg0;
+        const int ntiles = plan.item_page1[it] - plan.item_page0[it];
         for (int i = 0; i < ntiles; ++i, ++g) {
-          const int sb = g & 1;
-          if (!wait_phase(bar(SF0 + sb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          if (!wait_phase(bar(SF), g & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           uint32_t r[32];
-          tmem_ld32(tS + 64 * sb + 32 * peer, r);
+          tmem_ld32(tS + 32 * peer, r);
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(bar(SFREE0 + sb));
-          if (!wait_phase(bar(XE0 + sb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
-          if (g >= 2 && atid == 0) mbar_arrive_expect_tx(bar(XE0 + sb), kBWarps * 4);  // arm for page g+2
-          const uint32_t xa = r_x + sb * kXBytes + (uint32_t)row * 16;
-          const uint32_t xf = r_xf + 8u * sb;
+          mbar_arrive(bar(SFREE));
+          // the peer has read this CTA's partial of the previous page
+          if (g >= 1) {
+            if (!wait_phase(bar(XE), (g - 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            if (atid == 0) mbar_arrive_expect_tx(bar(XE), kBWarps * 4);  // arm for this page
+          }
+          const uint32_t xa = r_x + (uint32_t)row * 16;
+          const uint32_t xf = r_xf;
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
             uint4 w;
@@ -404,40 +396,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             w.w = cvt_f16x2(__uint_as_float(r[8 * q8 + 6]) * sl2, __uint_as_float(r[8 * q8 + 7]) * sl2);
             st_async_v4(xa + q8 * 128 * 16, w, xf);
           }
-          const int rows_valid = L - (pg0 + i) * kPage;
-          if (rows_valid < kPage) {
-            // slack rows past the context may hold any bits: zero this CTA's latent
-            // half so 0-weight x NaN cannot reach O (the score MMAs have read it)
-            const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
-            const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
-            for (int z = atid; z < nz; z += kAThreads) {
-              const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sa + cb * kCBoxBytes + rr * 128 + ch * 16),
-                           "r"(0u)
-                           : "memory");
-            }
-            fence_proxy_async_smem();
-          }
           // every score MMA of this range is done: stage the next range's query
           if (i == ntiles - 1 && it + 1 < it1) load_qc(it + 1);
-          if (++stage == kStages) stage = 0;
         }
       }
     } else {
       // -------------------------------------------------------- B: softmax + epilogue
-      // Warp w owns lane quadrant w % 4 and token quarter hf = (w - 6) / 4 of
+      // Warp w owns lane quadrant w % 4 and token quarter hf = (w - 7) / 4 of
       // this CTA's 32-token half of every page.
-      const int hf = (warp - 2 - kAWarps) >> 2;
-      const int btid = threadIdx.x - 64 - kAThreads;  // 0 .. 255
-      const int bwarp = warp - 2 - kAWarps;           // 0 .. 7
+      const int hf = (warp - 3 - kAWarps) >> 2;
+      const int btid = threadIdx.x - 96 - kAThreads;  // 0 .. 255
+      const int bwarp = warp - 3 - kAWarps;           // 0 .. 7
       const int mine0 = 32 * (int)rank + 16 * hf;     // first of this thread's 16 tokens in a page
       const uint32_t vec_off = (uint32_t)(hf * 128 + row) * 4;  // [2 quarters][128] float vectors
       const uint32_t vec_sib = (uint32_t)((hf ^ 1) * 128 + row) * 4;
-      const uint32_t prow_off = (uint32_t)row * 128;
-      auto pchunk = [&](int c) -> uint32_t { return prow_off + (uint32_t)((c ^ (row & 7)) * 16); };
       float x[16];
       float m_ref = -INFINITY, l_mine = 0.f;
-      int g = 0;
+      int g = 0, stage = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
@@ -449,22 +424,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           const int xb = g & 1;
           const bool first = (i == 0), last = (i == ntiles - 1);
           // this CTA's partial scores of this thread's 16 tokens
-          if (!wait_phase(bar(SF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          if (!wait_phase(bar(SF), g & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           {
             uint32_t r[16];
-            tmem_ld16(tS + 64 * xb + mine0, r);
+            tmem_ld16(tS + mine0, r);
             tmem_wait_ld();
 #pragma unroll
             for (int v = 0; v < 16; ++v) x[v] = __uint_as_float(r[v]) * sl2;
           }
           tc_fence_before();
-          mbar_arrive(bar(SFREE0 + xb));
+          mbar_arrive(bar(SFREE));
           // add the peer's partial for these tokens
-          if (!wait_phase(bar(XF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
-          if (btid == 0) mbar_arrive_expect_tx(bar(XF0 + xb), kXBytes);  // arm for page g+2
+          if (!wait_phase(bar(XF), g & 1, abort_flag, err_word)) { ok = false; break; }
+          if (btid == 0) mbar_arrive_expect_tx(bar(XF), kXBytes);  // arm for page g+1
           {
-            const uint32_t xa = sbase + kOffX + xb * kXBytes + (uint32_t)((2 * hf * 128 + row) * 16);
+            const uint32_t xa = sbase + kOffX + (uint32_t)((2 * hf * 128 + row) * 16);
 #pragma unroll
             for (int q8 = 0; q8 < 2; ++q8) {
               uint4 w;
@@ -482,7 +457,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           __syncwarp();
           // tell the peer this warp has read its partial (a 4-byte token completes
           // the peer's barrier; the loads above have all returned by now)
-          if (lane == 0) st_async_b32(r_tok + (uint32_t)(xb * kBWarps + bwarp) * 4, 1u, r_xe + 8u * xb);
+          if (lane == 0) st_async_b32(r_tok + (uint32_t)bwarp * 4, 1u, r_xe);
           const int nv = n_att - ((pg0 + i) * kPage + mine0);  // valid tokens among these 16
           if (nv < 16) {
 #pragma unroll
@@ -495,6 +470,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffMS + xb * kVec2Bytes + vec_off), "f"(m) : "memory");
           mbar_arrive(bar(MSF0 + xb));
           st_async_b32(r_mx + xb * kVec2Bytes + vec_off, __float_as_uint(m), r_mxf + 8u * xb);
+          const int rows_valid = L - (pg0 + i) * kPage;
+          if (rows_valid < kPage) {
+            // slack rows past the context may hold any bits: zero this CTA's latent
+            // half so 0-weight x NaN cannot reach O. The score MMAs have read the
+            // stage (SF); the value MMAs read it after this thread's P-ready arrive.
+            const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
+            const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
+            for (int z = btid; z < nz; z += kBThreads) {
+              const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sa + cb * kCBoxBytes + rr * 128 + ch * 16),
+                           "r"(0u)
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+          }
+          if (++stage == kStages) stage = 0;
           // the sibling warp's and the peer's page maxima
           if (!wait_phase(bar(MSF0 + xb), (g >> 1) & 1, abort_flag, err_word) ||
               !wait_phase(bar(MXF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
@@ -534,46 +525,45 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           // both CTAs' value MMAs of page g-2 have consumed this P buffer
           if (g >= 2 && !wait_phase(bar(PVD0 + xb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
           const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // all-masked so far: every p is 0
-          const uint32_t pl = sbase + kOffP + xb * kPBytes, pr = r_p + xb * kPBytes;
+          // this thread's 16 P values: into tensor memory for this CTA's value MMA
+          // and into the peer's shared memory (64B-swizzled, K-major) for its own
+          const uint32_t pr = r_p + xb * kPPeerBytes + (uint32_t)row * 64;
           const uint32_t pfr = r_pf + 8u * xb;
           float lsum0 = 0.f, lsum1 = 0.f;
+          uint32_t pw[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float p0 = ex2(x[2 * v] - mref);
+            const float p1 = ex2(x[2 * v + 1] - mref);
+            pw[v] = cvt_bf16x2(p0, p1);
+            lsum0 += bf16_lo(pw[v]);
+            lsum1 += bf16_hi(pw[v]);
+          }
+          tmem_st8(tmem + lane_off + kTmP + 16 * xb + 8 * hf, pw);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint4 w;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float p0 = ex2(x[8 * c + 2 * v] - mref);
-              const float p1 = ex2(x[8 * c + 2 * v + 1] - mref);
-              pw[v] = cvt_bf16x2(p0, p1);
-              lsum0 += bf16_lo(pw[v]);
-              lsum1 += bf16_hi(pw[v]);
-            }
-            const uint32_t off = pchunk((mine0 >> 3) + c);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(pl + off), "r"(w.x), "r"(w.y), "r"(w.z),
-                         "r"(w.w)
-                         : "memory");
-            st_async_v4(pr + off, w, pfr);
+            const int chunk = 2 * hf + c;  // 8-token chunk within this CTA's 32 tokens
+            st_async_v4(pr + (uint32_t)((chunk ^ ((row >> 1) & 3)) * 16),
+                        make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), pfr);
           }
+          tmem_wait_st();
           l_mine += lsum0 + lsum1;
           tc_fence_before();
           mbar_arrive(bar(PF0 + xb));
           if (last) {
             // softmax sum over the four token quarters, then the normalised output
-            const int lb = li & 1;
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffLS + lb * kVec2Bytes + vec_off), "f"(l_mine)
-                         : "memory");
-            mbar_arrive(bar(LSF0 + lb));
-            st_async_b32(r_lx + lb * kVec2Bytes + vec_off, __float_as_uint(l_mine), r_lxf + 8u * lb);
-            if (!wait_phase(bar(LSF0 + lb), (li >> 1) & 1, abort_flag, err_word) ||
-                !wait_phase(bar(LXF0 + lb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
-            if (btid == 0) mbar_arrive_expect_tx(bar(LXF0 + lb), kVec2Bytes);  // arm for range li+2
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffLS + vec_off), "f"(l_mine) : "memory");
+            mbar_arrive(bar(LSF));
+            st_async_b32(r_lx + vec_off, __float_as_uint(l_mine), r_lxf);
+            if (!wait_phase(bar(LSF), li & 1, abort_flag, err_word) ||
+                !wait_phase(bar(LXF), li & 1, abort_flag, err_word)) { ok = false; break; }
+            if (btid == 0) mbar_arrive_expect_tx(bar(LXF), kVec2Bytes);  // arm for the next range
             float a0, a1, b0, b1;  // this CTA's quarter sums, the peer's
             const uint32_t q0 = (uint32_t)row * 4, q1 = (uint32_t)(128 + row) * 4;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a0) : "r"(sbase + kOffLS + lb * kVec2Bytes + q0));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a1) : "r"(sbase + kOffLS + lb * kVec2Bytes + q1));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b0) : "r"(sbase + kOffLX + lb * kVec2Bytes + q0));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b1) : "r"(sbase + kOffLX + lb * kVec2Bytes + q1));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a0) : "r"(sbase + kOffLS + q0));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a1) : "r"(sbase + kOffLS + q1));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b0) : "r"(sbase + kOffLX + q0));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b1) : "r"(sbase + kOffLX + q1));
             // the same additions in the same order in both CTAs: rank 0's pair first
             const float l_tot = rank == 0 ? (a0 + a1) + (b0 + b1) : (b0 + b1) + (a0 + a1);
             if (!wait_phase(bar(PVD0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
