@@ -36,9 +36,10 @@
 //
 // Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
 // value-MMA issuer, 3..6 = score readers (the peer's tokens of S, the query
-// stage-in), 7..14 = softmax and epilogue, two warps per TMEM lane quadrant
-// (one thread per head row, 16 tokens each). The score MMAs of page g+1 run
-// while the softmax of page g is in flight; the value MMAs trail by one page.
+// stage-in), 7..14 = softmax and epilogue in two groups of four warps that
+// take alternate pages (one thread per head row, the CTA's 32 tokens of the
+// page). The score MMAs of page g+1 run while the softmax of page g is in
+// flight; the value MMAs trail by one page.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -49,8 +50,9 @@ using namespace sm100;
 
 constexpr int kStages = 5;
 constexpr int kAWarps = 4;  // score readers: one per TMEM lane quadrant
-constexpr int kBWarps = 8;  // softmax: two per lane quadrant, 16 tokens each
+constexpr int kBWarps = 8;  // softmax: two groups of four (one per lane quadrant), alternate pages
 constexpr int kAThreads = kAWarps * 32, kBThreads = kBWarps * 32;
+constexpr int kGThreads = kBThreads / 2;  // one softmax group: a thread per head row
 constexpr int kThreads = 96 + kAThreads + kBThreads;
 constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16, 128B swizzle
 constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
@@ -60,24 +62,27 @@ constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of
 constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads][32 tokens] bf16, 64B swizzle
 constexpr uint32_t kPHalfBytes = kPPeerBytes;
 constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
-constexpr uint32_t kVec2Bytes = 2 * kVecBytes;  // one float per head and token quarter
+constexpr uint32_t kTokBytes = 4 * 4;       // "partial consumed" tokens: one per warp of a group
 
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffQkr = kOffStage + kStages * kStageBytes;
 constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;   // peer partial scores (one page)
 constexpr uint32_t kOffP = kOffX + kXBytes;            // the peer's half of P, two pages
-constexpr uint32_t kOffMX = kOffP + 2 * kPPeerBytes;   // peer page maxima [2][2 quarters][128]
-constexpr uint32_t kOffMS = kOffMX + 2 * kVec2Bytes;   // this CTA's page maxima [2][2][128]
-constexpr uint32_t kOffLX = kOffMS + 2 * kVec2Bytes;   // peer softmax sums [2][128]
-constexpr uint32_t kOffLS = kOffLX + kVec2Bytes;       // this CTA's softmax sums [2][128]
-constexpr uint32_t kOffTok = kOffLS + kVec2Bytes;      // "partial consumed" tokens from the peer [8]
-constexpr uint32_t kOffBar = kOffTok + kBWarps * 4;
+constexpr uint32_t kOffMX = kOffP + 2 * kPPeerBytes;   // peer page maxima [2 pages][128]
+constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;    // peer softmax sums [2 ranges][128]
+constexpr uint32_t kOffMR = kOffLX + 2 * kVecBytes;    // reference maximum after the latest page [128]
+constexpr uint32_t kOffLG = kOffMR + kVecBytes;        // handed-over group sums [2 ranges][sum, ref][128]
+constexpr uint32_t kOffTok = kOffLG + 4 * kVecBytes;   // tokens from the peer
+constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 
-// barrier indices
+// barrier indices. A barrier that completes once per page and is waited by
+// only one of the two softmax groups exists once per group (index g % 2): a
+// parity wait is only sound if the barrier's previous phase is one this
+// waiter has already seen complete.
 enum {
   FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
-  SF = QCF + 1, SFREE = SF + 1, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF = PVD0 + 2, XE = XF + 1,
-  MXF0 = XE + 1, LXF = MXF0 + 2, MSF0 = LXF + 1, LSF = MSF0 + 2, OFREE = LSF + 1, MMAD = OFREE + 1,
+  SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
+  MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, OFREE = LGF0 + 2, MMAD = OFREE + 1,
   kNumBars = MMAD + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
@@ -117,29 +122,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(QKRF0 + i), 1);
       mbar_init(bar(QKRE0 + i), 1);
-      mbar_init(bar(PF0 + i), kBThreads + 1);  // local quarters + the arming arrive for the peer's half
+      mbar_init(bar(PF0 + i), kGThreads + 1);  // the group's rows + the arming arrive for the peer's half
       mbar_init(bar(PVD0 + i), 2);   // the value MMAs of this page done in both CTAs
       mbar_init(bar(MXF0 + i), 1);
-      mbar_init(bar(MSF0 + i), kBThreads);  // this CTA's page maxima written
+      mbar_init(bar(LXF0 + i), 1);
+      mbar_init(bar(LGF0 + i), kGThreads);  // a group's sums handed over
     }
-    mbar_init(bar(SF), 1);
-    mbar_init(bar(SFREE), kAThreads + kBThreads);
-    mbar_init(bar(XF), 1);   // armed here, filled by the peer's st.async
-    mbar_init(bar(XE), 1);   // armed here, completed by the peer's eight 4-byte tokens
-    mbar_init(bar(LXF), 1);
-    mbar_init(bar(LSF), kBThreads);  // this CTA's softmax sums written
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(SF0 + i), 1);
+      mbar_init(bar(XF0 + i), 1);  // armed here, filled by the peer's st.async
+    }
+    mbar_init(bar(SFREE), kAThreads + kGThreads);
+    mbar_init(bar(XE), 1);   // armed here, completed by the peer's four 4-byte tokens
+    mbar_init(bar(MRF), kGThreads);  // the reference maximum of a page posted
     mbar_init(bar(QCF), kAThreads);
-    mbar_init(bar(OFREE), kBThreads);
+    mbar_init(bar(OFREE), kGThreads);
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
     fence_mbar_init();
     for (int i = 0; i < 2; ++i) {
       mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
-      mbar_arrive_expect_tx(bar(MXF0 + i), kVec2Bytes);
+      mbar_arrive_expect_tx(bar(MXF0 + i), kVecBytes);
+      mbar_arrive_expect_tx(bar(LXF0 + i), kVecBytes);
+      mbar_arrive_expect_tx(bar(XF0 + i), kXBytes);
     }
-    mbar_arrive_expect_tx(bar(XF), kXBytes);
-    mbar_arrive_expect_tx(bar(XE), kBWarps * 4);
-    mbar_arrive_expect_tx(bar(LXF), kVec2Bytes);
+    mbar_arrive_expect_tx(bar(XE), kTokBytes);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_c);
@@ -289,7 +296,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             const uint64_t br = dQK_r + da(sbase + kOffStage + stage * kStageBytes + 4 * kCBoxBytes);
             mma_ss(d, ar, br, kIdQK, 1u);
             mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
-            mma_commit(bar(SF));
+            mma_commit(bar(SF0 + (g & 1)));
             if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
@@ -339,8 +346,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO, tQ = tmem + lane_off + kTmQ;
     const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
     const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
-    const uint32_t r_xf = mapa(bar(XF), peer), r_xe = mapa(bar(XE), peer), r_pf = mapa(bar(PF0), peer);
-    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF), peer);
+    const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE), peer), r_pf = mapa(bar(PF0), peer);
+    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF0), peer);
     const uint32_t r_tok = mapa(sbase + kOffTok, peer);
 
     if (warp < 3 + kAWarps) {
@@ -373,7 +380,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       for (int it = it0; it < it1 && ok; ++it) {
         const int ntiles = plan.item_page1[it] - plan.item_page0[it];
         for (int i = 0; i < ntiles; ++i, ++g) {
-          if (!wait_phase(bar(SF), g & 1, abort_flag, err_word)) { ok = false; break; }
+          if (!wait_phase(bar(SF0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           uint32_t r[32];
           tmem_ld32(tS + 32 * peer, r);
@@ -383,10 +390,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           // the peer has read this CTA's partial of the previous page
           if (g >= 1) {
             if (!wait_phase(bar(XE), (g - 1) & 1, abort_flag, err_word)) { ok = false; break; }
-            if (atid == 0) mbar_arrive_expect_tx(bar(XE), kBWarps * 4);  // arm for this page
+            if (atid == 0) mbar_arrive_expect_tx(bar(XE), kTokBytes);  // arm for this page
           }
           const uint32_t xa = r_x + (uint32_t)row * 16;
-          const uint32_t xf = r_xf;
+          const uint32_t xf = r_xf + 8u * (uint32_t)(g & 1);
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
             uint4 w;
@@ -402,17 +409,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       }
     } else {
       // -------------------------------------------------------- B: softmax + epilogue
-      // Warp w owns lane quadrant w % 4 and token quarter hf = (w - 7) / 4 of
-      // this CTA's 32-token half of every page.
-      const int hf = (warp - 3 - kAWarps) >> 2;
-      const int btid = threadIdx.x - 96 - kAThreads;  // 0 .. 255
-      const int bwarp = warp - 3 - kAWarps;           // 0 .. 7
-      const int mine0 = 32 * (int)rank + 16 * hf;     // first of this thread's 16 tokens in a page
-      const uint32_t vec_off = (uint32_t)(hf * 128 + row) * 4;  // [2 quarters][128] float vectors
-      const uint32_t vec_sib = (uint32_t)((hf ^ 1) * 128 + row) * 4;
-      float x[16];
-      float m_ref = -INFINITY, l_mine = 0.f;
-      int g = 0, stage = 0;
+      // Two groups of four warps (one per TMEM lane quadrant) take alternate
+      // pages: group grp handles the pages g with g % 2 == grp, one thread per
+      // head row and all 32 of this CTA's tokens of the page, so one group's
+      // exchanges with the peer overlap the other group's arithmetic. Through
+      // shared memory the groups pass the reference maximum of each head
+      // (decided page by page, in page order) and, at the end of a range, the
+      // softmax sum of the group that does not write the output.
+      const int grp = (warp - 3 - kAWarps) >> 2;
+      const int gwarp = (warp - 3 - kAWarps) & 3;
+      const int gtid = gwarp * 32 + lane;  // 0 .. 127
+      const uint32_t vec_off = (uint32_t)row * 4;
+      float x[32];
+      float l_g = 0.f, m_l = -INFINITY;  // this group's sum over the range so far, on reference m_l
+      int g = 0, lg_n = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
@@ -420,64 +430,66 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         const int L = plan.seq_len_eff[b];
         const int n_att = L - n_q + j + 1;
         const int ntiles = pg1 - pg0;
+        bool fresh = true;  // no page of this range handled by this group yet
         for (int i = 0; i < ntiles && ok; ++i, ++g) {
+          if ((g & 1) != grp) continue;
           const int xb = g & 1;
-          const bool first = (i == 0), last = (i == ntiles - 1);
-          // this CTA's partial scores of this thread's 16 tokens
-          if (!wait_phase(bar(SF), g & 1, abort_flag, err_word)) { ok = false; break; }
+          // this CTA's partial scores of its 32 tokens
+          if (!wait_phase(bar(SF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           {
-            uint32_t r[16];
-            tmem_ld16(tS + mine0, r);
+            uint32_t r[32];
+            tmem_ld32(tS + 32 * rank, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int v = 0; v < 16; ++v) x[v] = __uint_as_float(r[v]) * sl2;
+            for (int v = 0; v < 32; ++v) x[v] = __uint_as_float(r[v]) * sl2;
           }
           tc_fence_before();
           mbar_arrive(bar(SFREE));
           // add the peer's partial for these tokens
-          if (!wait_phase(bar(XF), g & 1, abort_flag, err_word)) { ok = false; break; }
-          if (btid == 0) mbar_arrive_expect_tx(bar(XF), kXBytes);  // arm for page g+1
-          {
-            const uint32_t xa = sbase + kOffX + (uint32_t)((2 * hf * 128 + row) * 16);
+          if (!wait_phase(bar(XF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          if (gtid == 0) mbar_arrive_expect_tx(bar(XF0 + xb), kXBytes);  // arm for page g+2
 #pragma unroll
-            for (int q8 = 0; q8 < 2; ++q8) {
-              uint4 w;
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w) : "r"(xa + q8 * 128 * 16));
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 w;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                         : "r"(sbase + kOffX + (uint32_t)((q8 * 128 + row) * 16)));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f = f16x2_to_f32(ww[k]);
-                x[8 * q8 + 2 * k] += f.x;
-                x[8 * q8 + 2 * k + 1] += f.y;
-              }
+            for (int k = 0; k < 4; ++k) {
+              const float2 f = f16x2_to_f32(ww[k]);
+              x[8 * q8 + 2 * k] += f.x;
+              x[8 * q8 + 2 * k + 1] += f.y;
             }
           }
           __syncwarp();
           // tell the peer this warp has read its partial (a 4-byte token completes
           // the peer's barrier; the loads above have all returned by now)
-          if (lane == 0) st_async_b32(r_tok + (uint32_t)bwarp * 4, 1u, r_xe);
-          const int nv = n_att - ((pg0 + i) * kPage + mine0);  // valid tokens among these 16
-          if (nv < 16) {
+          if (lane == 0) st_async_b32(r_tok + (uint32_t)gwarp * 4, 1u, r_xe);
+          const int nv = n_att - ((pg0 + i) * kPage + 32 * (int)rank);  // valid tokens among these 32
+          if (nv < 32) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
+            for (int jj = 0; jj < 32; ++jj)
               if (jj >= nv) x[jj] = -INFINITY;
           }
-          float m = fmaxf(x[0], x[1]);
+          // both CTAs' value MMAs of page g-2 are done: this group's P buffer is
+          // free, and the peer's page-max slot for this page was read (the peer
+          // reads it before its P-ready arrive of page g-2)
+          if (g >= 2 && !wait_phase(bar(PVD0 + xb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
+          float m = x[0];
 #pragma unroll
-          for (int jj = 2; jj < 16; ++jj) m = fmaxf(m, x[jj]);
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffMS + xb * kVec2Bytes + vec_off), "f"(m) : "memory");
-          mbar_arrive(bar(MSF0 + xb));
-          st_async_b32(r_mx + xb * kVec2Bytes + vec_off, __float_as_uint(m), r_mxf + 8u * xb);
+          for (int jj = 1; jj < 32; ++jj) m = fmaxf(m, x[jj]);
+          st_async_b32(r_mx + xb * kVecBytes + vec_off, __float_as_uint(m), r_mxf + 8u * xb);
           const int rows_valid = L - (pg0 + i) * kPage;
           if (rows_valid < kPage) {
             // slack rows past the context may hold any bits: zero this CTA's latent
             // half so 0-weight x NaN cannot reach O. The score MMAs have read the
-            // stage (SF); the value MMAs read it after this thread's P-ready arrive.
+            // stage (SF); the value MMAs read it after this group's P-ready arrive.
+            const int stage = g % kStages;
             const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
             const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
-            for (int z = btid; z < nz; z += kBThreads) {
+            for (int z = gtid; z < nz; z += kGThreads) {
               const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
               asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sa + cb * kCBoxBytes + rr * 128 + ch * 16),
                            "r"(0u)
@@ -485,96 +497,111 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             }
             fence_proxy_async_smem();
           }
-          if (++stage == kStages) stage = 0;
-          // the sibling warp's and the peer's page maxima
-          if (!wait_phase(bar(MSF0 + xb), (g >> 1) & 1, abort_flag, err_word) ||
-              !wait_phase(bar(MXF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
-          if (btid == 0) mbar_arrive_expect_tx(bar(MXF0 + xb), kVec2Bytes);  // arm for page g+2
-          float m_sib, m_p0, m_p1;
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_sib) : "r"(sbase + kOffMS + xb * kVec2Bytes + vec_sib));
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_p0) : "r"(sbase + kOffMX + xb * kVec2Bytes + vec_off));
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_p1) : "r"(sbase + kOffMX + xb * kVec2Bytes + vec_sib));
-          const float mt = fmaxf(fmaxf(m, m_sib), fmaxf(m_p0, m_p1));  // exact, identical everywhere
+          // the peer's page maximum: the exact page maximum, identical in both CTAs
+          if (!wait_phase(bar(MXF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          if (gtid == 0) mbar_arrive_expect_tx(bar(MXF0 + xb), kVecBytes);  // arm for page g+2
+          float m_p;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_p) : "r"(sbase + kOffMX + xb * kVecBytes + vec_off));
+          const float mt = fmaxf(m, m_p);
+          // the reference maximum: the previous page's decision (the other group's)
+          // is raised lazily, only when this page exceeds it by the threshold
+          if (g >= 1 && !wait_phase(bar(MRF), (g - 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          float m_new = mt, alpha = 1.f;
           bool need = false;
-          float alpha = 1.f;
-          if (first) {
-            m_ref = mt;
-            l_mine = 0.f;
-          } else if (mt > m_ref + kRescaleThreshold) {
-            alpha = ex2(m_ref - mt);
-            l_mine *= alpha;
-            m_ref = mt;
-            need = true;
+          if (i > 0) {
+            float m_prev;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_prev) : "r"(sbase + kOffMR + vec_off));
+            m_new = m_prev;
+            if (mt > m_prev + kRescaleThreshold) {
+              alpha = ex2(m_prev - mt);
+              m_new = mt;
+              need = true;
+            }
           }
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffMR + vec_off), "f"(m_new) : "memory");
+          mbar_arrive(bar(MRF));
           if (__any_sync(0xffffffffu, need)) {
-            // O must hold every earlier page before it is rescaled; this warp
-            // rescales its 128 of the 256 columns
-            if (!wait_phase(bar(PVD0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            // O must hold every earlier page before it is rescaled
+            if (!wait_phase(bar(PVD0 + (xb ^ 1)), ((g - 1) >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
-              tmem_ld32(tO + 128 * hf + 32 * c, r);
+              tmem_ld32(tO + 32 * c, r);
               tmem_wait_ld();
 #pragma unroll
               for (int v = 0; v < 32; ++v) r[v] = __float_as_uint(__uint_as_float(r[v]) * alpha);
-              tmem_st32(tO + 128 * hf + 32 * c, r);
+              tmem_st32(tO + 32 * c, r);
             }
-            tmem_wait_st();
           }
-          // both CTAs' value MMAs of page g-2 have consumed this P buffer
-          if (g >= 2 && !wait_phase(bar(PVD0 + xb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
-          const float mref = m_ref == -INFINITY ? 0.f : m_ref;  // all-masked so far: every p is 0
-          // this thread's 16 P values: into tensor memory for this CTA's value MMA
-          // and into the peer's shared memory (64B-swizzled, K-major) for its own
+          // this group's running sum, on the new reference
+          if (fresh) {
+            l_g = 0.f;
+            m_l = m_new;
+            fresh = false;
+          } else if (m_l != m_new) {
+            if (l_g != 0.f) l_g *= ex2(m_l - m_new);
+            m_l = m_new;
+          }
+          const float mref = m_new == -INFINITY ? 0.f : m_new;  // all masked so far: every p is 0
+          // P: into tensor memory for this CTA's value MMAs and into the peer's
+          // shared memory (64B-swizzled, K-major) for its own
           const uint32_t pr = r_p + xb * kPPeerBytes + (uint32_t)row * 64;
           const uint32_t pfr = r_pf + 8u * xb;
           float lsum0 = 0.f, lsum1 = 0.f;
-          uint32_t pw[8];
+          uint32_t pw[16];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
+          for (int v = 0; v < 16; ++v) {
             const float p0 = ex2(x[2 * v] - mref);
             const float p1 = ex2(x[2 * v + 1] - mref);
             pw[v] = cvt_bf16x2(p0, p1);
             lsum0 += bf16_lo(pw[v]);
             lsum1 += bf16_hi(pw[v]);
           }
-          tmem_st8(tmem + lane_off + kTmP + 16 * xb + 8 * hf, pw);
+          tmem_st16(tmem + lane_off + kTmP + 16 * xb, pw);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int chunk = 2 * hf + c;  // 8-token chunk within this CTA's 32 tokens
-            st_async_v4(pr + (uint32_t)((chunk ^ ((row >> 1) & 3)) * 16),
+          for (int c = 0; c < 4; ++c)
+            st_async_v4(pr + (uint32_t)((c ^ ((row >> 1) & 3)) * 16),
                         make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]), pfr);
-          }
           tmem_wait_st();
-          l_mine += lsum0 + lsum1;
+          l_g += lsum0 + lsum1;
           tc_fence_before();
           mbar_arrive(bar(PF0 + xb));
-          if (last) {
-            // softmax sum over the four token quarters, then the normalised output
-            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffLS + vec_off), "f"(l_mine) : "memory");
-            mbar_arrive(bar(LSF));
-            st_async_b32(r_lx + vec_off, __float_as_uint(l_mine), r_lxf);
-            if (!wait_phase(bar(LSF), li & 1, abort_flag, err_word) ||
-                !wait_phase(bar(LXF), li & 1, abort_flag, err_word)) { ok = false; break; }
-            if (btid == 0) mbar_arrive_expect_tx(bar(LXF), kVec2Bytes);  // arm for the next range
-            float a0, a1, b0, b1;  // this CTA's quarter sums, the peer's
-            const uint32_t q0 = (uint32_t)row * 4, q1 = (uint32_t)(128 + row) * 4;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a0) : "r"(sbase + kOffLS + q0));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a1) : "r"(sbase + kOffLS + q1));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b0) : "r"(sbase + kOffLX + q0));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(b1) : "r"(sbase + kOffLX + q1));
-            // the same additions in the same order in both CTAs: rank 0's pair first
-            const float l_tot = rank == 0 ? (a0 + a1) + (b0 + b1) : (b0 + b1) + (a0 + a1);
+          if (i == ntiles - 2) {
+            // the other group handles the last page of the range: hand over this sum
+            const uint32_t lg = sbase + kOffLG + (uint32_t)(lg_n & 1) * 2 * kVecBytes;
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(lg + vec_off), "f"(l_g) : "memory");
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(lg + kVecBytes + vec_off), "f"(m_l) : "memory");
+            mbar_arrive(bar(LGF0 + (lg_n & 1)));
+          }
+          if (i == ntiles - 1) {
+            // epilogue: the CTA's sum (both groups), the peer's, the normalised output
+            float l_c = l_g;
+            if (ntiles >= 2) {
+              if (!wait_phase(bar(LGF0 + (lg_n & 1)), (lg_n >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+              const uint32_t lg = sbase + kOffLG + (uint32_t)(lg_n & 1) * 2 * kVecBytes;
+              float l_o, m_o;
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l_o) : "r"(lg + vec_off));
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_o) : "r"(lg + kVecBytes + vec_off));
+              if (l_o != 0.f) l_c += l_o * ex2(m_o - m_new);
+            }
+            const int lb = li & 1;
+            st_async_b32(r_lx + lb * kVecBytes + vec_off, __float_as_uint(l_c), r_lxf + 8u * lb);
+            if (!wait_phase(bar(LXF0 + lb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            if (gtid == 0) mbar_arrive_expect_tx(bar(LXF0 + lb), kVecBytes);  // arm for range li+2
+            float l_p;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l_p) : "r"(sbase + kOffLX + lb * kVecBytes + vec_off));
+            // the same addition in the same order in both CTAs: rank 0's sum first
+            const float l_tot = rank == 0 ? l_c + l_p : l_p + l_c;
             if (!wait_phase(bar(PVD0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
             const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const size_t orow = ((size_t)it * n_q + j) * H + row;
-            float4* dst = reinterpret_cast<float4*>(plan.o_part + orow * kDC + 256 * rank + 128 * hf);
+            float4* dst = reinterpret_cast<float4*>(plan.o_part + orow * kDC + 256 * rank);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 8; ++c) {
               uint32_t r[32];
-              tmem_ld32(tO + 128 * hf + 32 * c, r);
+              tmem_ld32(tO + 32 * c, r);
               tmem_wait_ld();
               if (row < H) {
 #pragma unroll
@@ -586,10 +613,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             }
             tc_fence_before();
             mbar_arrive(bar(OFREE));
-            if (rank == 0 && hf == 0 && row < H)
-              plan.lse_part[orow] = l_tot > 0.f ? (m_ref + log2f(l_tot)) * kLn2 : -INFINITY;
+            if (rank == 0 && row < H)
+              plan.lse_part[orow] = l_tot > 0.f ? (m_new + log2f(l_tot)) * kLn2 : -INFINITY;
           }
         }
+        if (ntiles >= 2) ++lg_n;
       }
     }
   }
