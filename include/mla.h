@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 #define MLA_MAX_BATCH 4096
 
 typedef enum {
@@ -108,7 +108,9 @@ mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const ui
  *   seq_len_eff[B]          the context lengths actually used (clamped)
  *   item_seq[I], item_page0[I], item_page1[I]   sequence and page range
  *   lse_part[I][n_q][H]     float, natural-log sum-exp of the range's scores
- *   o_part[I][n_q][H][512]  float, the range's softmax-normalised sum of latents
+ *   o_part[I][n_q][128][H][4] float, the range's softmax-normalised sum of
+ *                           latents, head-minor in groups of four columns:
+ *                           o_part[k][j][c / 4][h][c % 4] is column c of head h
  */
 int mla_decode_default_splits(int n_q);
 size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);

@@ -2,9 +2,11 @@
 // Dev Blog "MLA 아키텍처 해부" section 4 table names FlashDecoding as the
 // decode technique):
 //   lse = ln sum_k exp(lse_k),   u = sum_k exp(lse_k - lse) * o_k
-// One warp per (sequence, query, head); each lane owns 16 of the 512 latent
-// columns as four float4 groups, so partial reads are 128-bit and coalesced,
-// and each lane writes 8 bytes of bf16 output per group.
+// One block per (sequence, query) row and 32-column slice, two threads per
+// head (16 columns each); the loads of four partials are in flight together. The partials are head-minor in groups of four columns
+// (o_part[k][j][column / 4][head][column % 4]), so a warp reads 32
+// consecutive heads of four columns as one 512-byte run; the bf16 result goes
+// through shared memory so the stores of u are row-contiguous.
 #include "mla_internal.cuh"
 
 #include "sm100.cuh"
@@ -12,75 +14,86 @@
 namespace mla {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kThreads = 256;  // two per head (H <= 128): 16 columns each
+constexpr int kCols = 32;      // latent columns per block
+constexpr int kKB = 4;         // partials whose loads are in flight together
 
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads)
 combine_kernel(Plan plan, int n_q, int H, uint16_t* __restrict__ u, float* __restrict__ lse_out) {
+  __shared__ uint32_t tile[128][kCols / 2 + 1];  // bf16 pairs, padded row
   sm100::grid_dependency_wait();  // the partials come from the decode kernel
   sm100::grid_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = threadIdx.x & 127, part = threadIdx.x >> 7;
   const int bj = blockIdx.x;  // b * n_q + j
-  const int h = blockIdx.y * kWarps + warp;
-  if (h >= H) return;
+  const int c0 = blockIdx.y * kCols + 16 * part;  // this thread's first column
   const int b = bj / n_q, j = bj % n_q;
   const int k0 = plan.seq_item[b], k1 = plan.seq_item[b + 1];
-  auto row_of = [&](int k) { return ((size_t)k * n_q + j) * H + h; };
-
-  // all log-sum-exps of this row at once: lane l holds piece k0 + 32 i + l
-  float m = -INFINITY;
-  for (int k = k0 + lane; k < k1; k += 32) m = fmaxf(m, plan.lse_part[row_of(k)]);
+  auto lse_of = [&](int k) { return plan.lse_part[((size_t)k * n_q + j) * H + h]; };
+  float acc[16];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float4 acc[4];
+  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+  float m = -INFINITY, wsum = 0.f;
+  if (h < H) {
+    // the maximum log-sum-exp, eight independent loads at a time
+    for (int kb = k0; kb < k1; kb += 8) {
+      float l[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (m != -INFINITY) {
-    for (int kc = k0; kc < k1; kc += 32) {
-      const int n = min(32, k1 - kc);
-      const float lk = lane < n ? plan.lse_part[row_of(kc + lane)] : -INFINITY;
-      const float wl = lk == -INFINITY ? 0.f : expf(lk - m);
-      float ws = wl;
+      for (int i = 0; i < 8; ++i) l[i] = kb + i < k1 ? lse_of(kb + i) : -INFINITY;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-      wsum += ws;
-#pragma unroll 4
-      for (int k = 0; k < n; ++k) {
-        const float w = __shfl_sync(0xffffffffu, wl, k);
-        const float4* src = reinterpret_cast<const float4*>(plan.o_part + row_of(kc + k) * kDC);
-        float4 v[4];
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, l[i]);
+    }
+    if (m != -INFINITY) {
+      for (int kb = k0; kb < k1; kb += kKB) {
+        float w[kKB];
+        float4 v[kKB][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = src[lane + 32 * i];
-        if (w != 0.f) {
+        for (int i = 0; i < kKB; ++i) {
+          const int k = kb + i;
+          const float lk = k < k1 ? lse_of(k) : -INFINITY;
+          w[i] = lk == -INFINITY ? 0.f : expf(lk - m);
+          const float4* src = reinterpret_cast<const float4*>(plan.o_part) +
+                              (((size_t)min(k, k1 - 1) * n_q + j) * (kDC / 4) + c0 / 4) * H + h;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[i].x = fmaf(w, v[i].x, acc[i].x);
-            acc[i].y = fmaf(w, v[i].y, acc[i].y);
-            acc[i].z = fmaf(w, v[i].z, acc[i].z);
-            acc[i].w = fmaf(w, v[i].w, acc[i].w);
+          for (int q = 0; q < 4; ++q) v[i][q] = k < k1 ? src[(size_t)q * H] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kKB; ++i) {
+          wsum += w[i];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[4 * q] = fmaf(w[i], v[i][q].x, acc[4 * q]);
+            acc[4 * q + 1] = fmaf(w[i], v[i][q].y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(w[i], v[i][q].z, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(w[i], v[i][q].w, acc[4 * q + 3]);
           }
         }
       }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint2* dst = reinterpret_cast<uint2*>(u + ((size_t)bj * H + h) * kDC);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint2 o;
-    o.x = pack_bf16x2(acc[i].x * inv, acc[i].y * inv);
-    o.y = pack_bf16x2(acc[i].z * inv, acc[i].w * inv);
-    dst[lane + 32 * i] = o;
+  for (int c = 0; c < 8; ++c) tile[h][8 * part + c] = pack_bf16x2(acc[2 * c] * inv, acc[2 * c + 1] * inv);
+  __syncthreads();
+  // row h of the slice is 64 contiguous bytes of u: 4 threads per row, 16 bytes each
+  for (int i = threadIdx.x; i < H * 4; i += kThreads) {
+    const int row = i >> 2, q = i & 3;
+    uint4 o;
+    o.x = tile[row][4 * q];
+    o.y = tile[row][4 * q + 1];
+    o.z = tile[row][4 * q + 2];
+    o.w = tile[row][4 * q + 3];
+    *reinterpret_cast<uint4*>(u + ((size_t)bj * H + row) * kDC + blockIdx.y * kCols + 8 * q) = o;
   }
-  if (lse_out && lane == 0) lse_out[(size_t)bj * H + h] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  if (lse_out && blockIdx.y == 0 && part == 0 && h < H)
+    lse_out[(size_t)bj * H + h] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const Plan& plan, int B, int n_q, int H, uint16_t* u, float* lse,
                            cudaStream_t s) {
-  dim3 grid(B * n_q, (H + kWarps - 1) / kWarps);
-  return launch_pdl(combine_kernel, grid, dim3(kWarps * 32), 0, s, plan, n_q, H, u, lse);
+  dim3 grid(B * n_q, kDC / kCols);
+  return launch_pdl(combine_kernel, grid, dim3(kThreads), 0, s, plan, n_q, H, u, lse);
 }
 
 }  // namespace mla

@@ -72,7 +72,8 @@ constexpr uint32_t kOffMX = kOffP + 2 * kPPeerBytes;   // peer page maxima [2 pa
 constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;    // peer softmax sums [2 ranges][128]
 constexpr uint32_t kOffMR = kOffLX + 2 * kVecBytes;    // reference maximum after the latest page [128]
 constexpr uint32_t kOffLG = kOffMR + kVecBytes;        // handed-over group sums [2 ranges][sum, ref][128]
-constexpr uint32_t kOffTok = kOffLG + 4 * kVecBytes;   // tokens from the peer
+constexpr uint32_t kOffIV = kOffLG + 4 * kVecBytes;    // 1 / softmax sum of the range [128]
+constexpr uint32_t kOffTok = kOffIV + kVecBytes;       // tokens from the peer
 constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 
 // barrier indices. A barrier that completes once per page and is waited by
@@ -82,7 +83,8 @@ constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 enum {
   FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
   SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
-  MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, OFREE = LGF0 + 2, MMAD = OFREE + 1,
+  MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
+  MMAD = OFREE + 1,
   kNumBars = MMAD + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
@@ -127,6 +129,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_init(bar(MXF0 + i), 1);
       mbar_init(bar(LXF0 + i), 1);
       mbar_init(bar(LGF0 + i), kGThreads);  // a group's sums handed over
+      mbar_init(bar(IVF0 + i), kGThreads);  // 1/l posted for helper group i
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SF0 + i), 1);
@@ -135,8 +138,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     mbar_init(bar(SFREE), kAThreads + kGThreads);
     mbar_init(bar(XE), 1);   // armed here, completed by the peer's four 4-byte tokens
     mbar_init(bar(MRF), kGThreads);  // the reference maximum of a page posted
-    mbar_init(bar(QCF), kAThreads);
-    mbar_init(bar(OFREE), kGThreads);
+    mbar_init(bar(QCF), kAThreads + kGThreads);  // query halves: score readers + the helper group
+    mbar_init(bar(OFREE), 2 * kGThreads);        // both halves of O drained
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
     fence_mbar_init();
@@ -356,20 +359,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       // them (log2 units, fp16) into the peer's shared memory, zero slack rows,
       // and stage the query of the next range.
       const int atid = threadIdx.x - 96;  // 0 .. 127
+      // the range's latent query half, columns [0, 64) of tensor memory Q (the
+      // helper softmax group stores [64, 128)); one batch of 16 loads per thread
       auto load_qc = [&](int it) {
         const int b = plan.item_seq[it];
         const size_t qrow = ((size_t)b * n_q + j) * H + row;
         const uint4* src = reinterpret_cast<const uint4*>(q_abs + qrow * kRow + 256 * rank);
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
+        uint32_t r0[32], r1[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint4 w = row < H ? __ldg(src + c * 8 + v) : make_uint4(0, 0, 0, 0);
-            r[4 * v] = w.x; r[4 * v + 1] = w.y; r[4 * v + 2] = w.z; r[4 * v + 3] = w.w;
-          }
-          tmem_st32(tQ + 32 * c, r);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w0 = row < H ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          const uint4 w1 = row < H ? __ldg(src + 8 + v) : make_uint4(0, 0, 0, 0);
+          r0[4 * v] = w0.x; r0[4 * v + 1] = w0.y; r0[4 * v + 2] = w0.z; r0[4 * v + 3] = w0.w;
+          r1[4 * v] = w1.x; r1[4 * v + 1] = w1.y; r1[4 * v + 2] = w1.z; r1[4 * v + 3] = w1.w;
         }
+        tmem_st32(tQ, r0);
+        tmem_st32(tQ + 32, r1);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(QCF));
@@ -422,8 +427,54 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       const uint32_t vec_off = (uint32_t)row * 4;
       float x[32];
       float l_g = 0.f, m_l = -INFINITY;  // this group's sum over the range so far, on reference m_l
-      int g = 0, lg_n = 0;
+      int g = 0, lg_n = 0, iv_n = 0;
       bool ok = true;
+      // The group that does not handle a range's last page helps at the range
+      // switch: it stores columns [64, 128) of the next range's query half
+      // (issuing the loads before the last score MMA completes) and drains
+      // columns [128, 256) of O once the other group has posted 1/l.
+      auto q_loads = [&](int it, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+        const size_t qrow = ((size_t)plan.item_seq[it] * n_q + j) * H + row;
+        const uint4* src = reinterpret_cast<const uint4*>(q_abs + qrow * kRow + 256 * rank + 128);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w0 = row < H ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+          const uint4 w1 = row < H ? __ldg(src + 8 + v) : make_uint4(0, 0, 0, 0);
+          r0[4 * v] = w0.x; r0[4 * v + 1] = w0.y; r0[4 * v + 2] = w0.z; r0[4 * v + 3] = w0.w;
+          r1[4 * v] = w1.x; r1[4 * v + 1] = w1.y; r1[4 * v + 2] = w1.z; r1[4 * v + 3] = w1.w;
+        }
+      };
+      auto q_store = [&](const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
+        tmem_st32(tQ + 64, r0);
+        tmem_st32(tQ + 96, r1);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(QCF));
+      };
+      // O columns [128 h, 128 h + 128) of this CTA's half, scaled by inv, into the
+      // head-minor partials o_part[item][j][column / 4][head][column % 4]
+      auto drain_o = [&](int it, int half, float inv) {
+        float4* dst = reinterpret_cast<float4*>(plan.o_part) +
+                      ((size_t)(it * n_q + j) * (kDC / 4) + (256 * rank + 128 * half) / 4) * H + row;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 128 * half + 32 * c, r);
+          tmem_wait_ld();
+          if (row < H) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[(size_t)(8 * c + v) * H] =
+                  make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                              __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+      };
+      if (grp == 1 && it0 < it1) {
+        uint32_t r0[32], r1[32];
+        q_loads(it0, r0, r1);
+        q_store(r0, r1);
+      }
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
         const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
@@ -432,7 +483,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         const int ntiles = pg1 - pg0;
         bool fresh = true;  // no page of this range handled by this group yet
         for (int i = 0; i < ntiles && ok; ++i, ++g) {
-          if ((g & 1) != grp) continue;
+          if ((g & 1) != grp) {
+            if (i == ntiles - 1) {
+              // helper at the end of the range handled by the other group
+              if (it + 1 < it1) {
+                uint32_t r0[32], r1[32];
+                q_loads(it + 1, r0, r1);
+                // the range's last score MMA has read tensor-memory Q (the other
+                // group's barrier: its previous phase, page g-2, completed before
+                // the other group posted the reference maximum of page g-2)
+                if (!wait_phase(bar(SF0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+                tc_fence_after();
+                q_store(r0, r1);
+              }
+              if (!wait_phase(bar(IVF0 + grp), iv_n & 1, abort_flag, err_word)) { ok = false; break; }
+              ++iv_n;
+              float inv;
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv) : "r"(sbase + kOffIV + vec_off));
+              if (!wait_phase(bar(PVD0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+              tc_fence_after();
+              drain_o(it, 1, inv);
+              tc_fence_before();
+              mbar_arrive(bar(OFREE));
+            }
+            continue;
+          }
           const int xb = g & 1;
           // this CTA's partial scores of its 32 tokens
           if (!wait_phase(bar(SF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
@@ -593,24 +668,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l_p) : "r"(sbase + kOffLX + lb * kVecBytes + vec_off));
             // the same addition in the same order in both CTAs: rank 0's sum first
             const float l_tot = rank == 0 ? l_c + l_p : l_p + l_c;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            // 1/l for the helper group, which drains the other half of O
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffIV + vec_off), "f"(inv) : "memory");
+            mbar_arrive(bar(IVF0 + (grp ^ 1)));
             if (!wait_phase(bar(PVD0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const size_t orow = ((size_t)it * n_q + j) * H + row;
-            float4* dst = reinterpret_cast<float4*>(plan.o_part + orow * kDC + 256 * rank);
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t r[32];
-              tmem_ld32(tO + 32 * c, r);
-              tmem_wait_ld();
-              if (row < H) {
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                  dst[c * 8 + v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                               __uint_as_float(r[4 * v + 2]) * inv,
-                                               __uint_as_float(r[4 * v + 3]) * inv);
-              }
-            }
+            drain_o(it, 0, inv);
             tc_fence_before();
             mbar_arrive(bar(OFREE));
             if (rank == 0 && row < H)

@@ -93,14 +93,14 @@ def test_combine_alone_merges_oracle_partials(mla):
     host = np.zeros(ws.numel(), dtype=np.uint8)
     host[offs[2]:offs[2] + (inp.B + 1) * 4] = pl["seq_item"].astype(np.int32).view(np.uint8)
     lse_part = np.full((I, inp.n_q, inp.H), -np.inf, dtype=np.float32)
-    o_part = np.zeros((I, inp.n_q, inp.H, 512), dtype=np.float32)
+    o_part = np.zeros((I, inp.n_q, 128, inp.H, 4), dtype=np.float32)  # [c/4][h][c%4]
     rows = np.arange(inp.B * inp.n_q * inp.H)
     for k, (b, p0, p1) in enumerate(pl["items"]):
         part = oracle.split_partials_f64(inp, [[p0 * 64, p1 * 64]], rows)
         for j in range(inp.n_q):
             r = (b * inp.n_q + j) * inp.H + np.arange(inp.H)
             lse_part[k, j] = part["lse"][r, 0]
-            o_part[k, j] = part["u"][r, 0]
+            o_part[k, j] = part["u"][r, 0].reshape(inp.H, 128, 4).transpose(1, 0, 2)
     host[offs[7]:offs[7] + lse_part.nbytes] = lse_part.view(np.uint8).ravel()
     host[offs[8]:offs[8] + o_part.nbytes] = o_part.view(np.uint8).ravel()
     ws.copy_(torch.from_numpy(host))
