@@ -43,7 +43,8 @@ struct ProjCfg {
 template <bool kAbsorb, int kNT>
 __global__ void __launch_bounds__(kThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const uint16_t* __restrict__ q_rope, uint16_t* __restrict__ out, int T, int H, int32_t* err_word) {
+               const uint16_t* __restrict__ weights, const uint16_t* __restrict__ q_rope, uint16_t* __restrict__ out,
+               int T, int H, int32_t* err_word) {
   using C = ProjCfg<kAbsorb, kNT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -63,6 +64,9 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     fence_mbar_init();
     prefetch_tmap(&map_a);
     prefetch_tmap(&map_b);
+    // this head's weights into L2 while the previous kernel finishes (one CTA
+    // per head for absorb_q, whose four column blocks share them)
+    if (!kAbsorb || cblk == 0) bulk_prefetch_l2(weights + (size_t)h * 128 * kDC, 128 * kDC * 2);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmCols);
@@ -166,8 +170,8 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 }
 
 template <bool kAbsorb, int kNT>
-cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint16_t* q_rope, uint16_t* out,
-                        int T, int H, cudaStream_t s) {
+cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint16_t* w, const uint16_t* q_rope,
+                        uint16_t* out, int T, int H, cudaStream_t s) {
   using C = ProjCfg<kAbsorb, kNT>;
   static bool done = false;
   if (!done) {
@@ -177,8 +181,8 @@ cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint
     done = true;
   }
   const dim3 grid(H, kAbsorb ? kDC / 128 : 1);
-  return launch_pdl(proj_tc_kernel<kAbsorb, kNT>, grid, dim3(kThreads), C::kSmem, s, ma, mb, q_rope, out, T, H,
-                    (int32_t*)nullptr);
+  return launch_pdl(proj_tc_kernel<kAbsorb, kNT>, grid, dim3(kThreads), C::kSmem, s, ma, mb, w, q_rope, out, T,
+                    H, (int32_t*)nullptr);
 }
 
 bool maps(CUtensorMap* ma, CUtensorMap* mb, const uint16_t* w, const uint16_t* act, int T, int H, int K, int nt) {
@@ -196,9 +200,9 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, cons
   const int nt = T <= 32 ? 32 : T <= 64 ? 64 : 128;
   CUtensorMap ma, mb;
   if (!maps(&ma, &mb, w_uk, q_nope, T, H, kDNope, nt)) return cudaErrorInvalidValue;
-  if (nt == 32) return launch_proj<true, 32>(ma, mb, q_rope, q_abs, T, H, s);
-  if (nt == 64) return launch_proj<true, 64>(ma, mb, q_rope, q_abs, T, H, s);
-  return launch_proj<true, 128>(ma, mb, q_rope, q_abs, T, H, s);
+  if (nt == 32) return launch_proj<true, 32>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
+  if (nt == 64) return launch_proj<true, 64>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
+  return launch_proj<true, 128>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
 }
 
 cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
@@ -206,8 +210,8 @@ cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* o
   const int nt = T <= 32 ? 32 : 64;
   CUtensorMap ma, mb;
   if (!maps(&ma, &mb, w_uv, u, T, H, kDC, nt)) return cudaErrorInvalidValue;
-  if (nt == 32) return launch_proj<false, 32>(ma, mb, nullptr, out, T, H, s);
-  return launch_proj<false, 64>(ma, mb, nullptr, out, T, H, s);
+  if (nt == 32) return launch_proj<false, 32>(ma, mb, w_uv, nullptr, out, T, H, s);
+  return launch_proj<false, 64>(ma, mb, w_uv, nullptr, out, T, H, s);
 }
 
 }  // namespace mla

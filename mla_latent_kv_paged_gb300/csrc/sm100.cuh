@@ -117,6 +117,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---------------------------------------------------------------- TMA
 // Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+// A hint only: L2 stays coherent, so it is safe before a grid dependency wait.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                : "memory");
