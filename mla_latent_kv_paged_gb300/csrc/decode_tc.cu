@@ -30,16 +30,18 @@
 //
 // Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S [256,320),
 // this CTA's P half for two pages [320,352), the CTA's latent half of q_abs as
-// the score MMAs' A operand [384,512). Shared memory: 5-stage page ring
-// (180 KB), the positional half of q_abs (2 x 8 KB), the peer's partial
-// scores (8 KB), the peer's P half (2 x 8 KB), the exchange vectors.
+// the score MMAs' A operand [384,512). Shared memory: 5-slot ring (180 KB) of
+// page halves and, at the start of each range, the latent query half (TMA into
+// two slots, then tcgen05.cp into tensor memory), the positional half of q_abs
+// (2 x 8 KB), the peer's partial scores (8 KB), the peer's P half (2 x 8 KB),
+// the exchange vectors.
 //
 // Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
-// value-MMA issuer, 3..6 = score readers (the peer's tokens of S, the query
-// stage-in), 7..14 = softmax and epilogue in two groups of four warps that
-// take alternate pages (one thread per head row, the CTA's 32 tokens of the
-// page). The score MMAs of page g+1 run while the softmax of page g is in
-// flight; the value MMAs trail by one page.
+// value-MMA issuer, 3..6 = score readers (the peer's tokens of S), 7..14 =
+// softmax and epilogue in two groups of four warps that take alternate pages
+// (one thread per head row, the CTA's 32 tokens of the page). The score MMAs
+// of page g+1 run while the softmax of page g is in flight; the value MMAs
+// trail by one page.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -58,6 +60,8 @@ constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16,
 constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
 constexpr uint32_t kQkrBytes = 128 * 64;    // [128 heads][32] bf16, 64B swizzle
+constexpr uint32_t kQBoxBytes = 128 * 128;  // [128 heads][64 latent cols] bf16, 128B swizzle
+constexpr int kQSlots = 2;                  // ring slots taken by a range's latent query half (4 boxes)
 constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of 8 tokens][128 heads] fp16
 constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads][32 tokens] bf16, 64B swizzle
 constexpr uint32_t kPHalfBytes = kPPeerBytes;
@@ -81,8 +85,8 @@ constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 // parity wait is only sound if the barrier's previous phase is one this
 // waiter has already seen complete.
 enum {
-  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
-  SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
+  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QDONE = QKRE0 + 2,
+  SF0 = QDONE + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
   MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
   MMAD = OFREE + 1,
   kNumBars = MMAD + 1
@@ -100,7 +104,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
-                 const __grid_constant__ CUtensorMap map_qkr, const uint16_t* __restrict__ q_abs,
+                 const __grid_constant__ CUtensorMap map_qkr, const __grid_constant__ CUtensorMap map_q,
                  const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, int num_pages,
                  float sl2, Plan plan, int32_t* err_word) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -138,7 +142,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     mbar_init(bar(SFREE), kAThreads + kGThreads);
     mbar_init(bar(XE), 1);   // armed here, completed by the peer's four 4-byte tokens
     mbar_init(bar(MRF), kGThreads);  // the reference maximum of a page posted
-    mbar_init(bar(QCF), kAThreads + kGThreads);  // query halves: score readers + the helper group
+    mbar_init(bar(QDONE), 1);  // every score MMA of a range done: tensor-memory Q may be replaced
     mbar_init(bar(OFREE), 2 * kGThreads);        // both halves of O drained
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
@@ -155,6 +159,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     prefetch_tmap(&map_c);
     prefetch_tmap(&map_kr);
     prefetch_tmap(&map_qkr);
+    prefetch_tmap(&map_q);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmCols);
@@ -222,6 +227,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
                       (plan.item_seq[it] * n_q + j) * H, pol_keep);
         }
         last_qph[qb] = (li >> 1) & 1;
+        // and its latent half, four [128 heads][64] boxes into the next two ring
+        // slots; the score-MMA issuer copies them into tensor memory
+        const int qrow = (plan.item_seq[it] * n_q + j) * H;
+        for (int q = 0; q < kQSlots && ok; ++q) {
+          if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
+          if (lane == 0) {
+            const uint32_t fb = bar(FULL0 + stage);
+            const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
+            mbar_arrive_expect_tx(fb, 2 * kQBoxBytes);
+            for (int m = 0; m < 2; ++m)
+              tma_load_2d(dst + m * kQBoxBytes, &map_q, fb, 256 * (int)rank + 128 * q + 64 * m, qrow, pol_keep);
+          }
+          last_ph[stage] = (int)ph;
+          __syncwarp();
+          if (++stage == kStages) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
       }
       const int pid = cur_next(ld);
       // an id outside the pool loads zeros (TMA bounds) and is reported
@@ -282,9 +304,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0, qb = li & 1;
           const int ntiles = plan.item_page1[it] - plan.item_page0[it];
-          // the range's query: latent half in tensor memory, positional half by TMA
-          if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word) ||
-              !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          // the range's query: the latent half from its two ring slots into
+          // tensor memory (once every score MMA of the previous range is done),
+          // the positional half stays in shared memory
+          if (li > 0 && !wait_phase(bar(QDONE), (li - 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          for (int q = 0; q < kQSlots && ok; ++q) {
+            if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sq = sbase + kOffStage + stage * kStageBytes;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)  // 16 bf16 (32 bytes) of each row per copy
+              tmem_cp_128x256b(tmem + kTmQ + 64 * q + 8 * k,
+                               dQK_c + da(sq + (k >> 2) * kQBoxBytes + (k & 3) * 32));
+            mma_commit(bar(EMPTY0 + stage));  // the slot is free once the copies are done
+            if (++stage == kStages) { stage = 0; ph ^= 1u; }
+          }
+          if (!ok || !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           for (int i = 0; i < ntiles; ++i, ++g) {
             if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
                 !wait_phase(bar(SFREE), (g & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
@@ -300,7 +335,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             mma_ss(d, ar, br, kIdQK, 1u);
             mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
             mma_commit(bar(SF0 + (g & 1)));
-            if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
+            if (i == ntiles - 1) {
+              mma_commit(bar(QKRE0 + qb));
+              mma_commit(bar(QDONE));
+            }
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
         }
@@ -310,6 +348,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0;
           const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+          for (int q = 0; q < kQSlots; ++q)  // the range's query slots (released by the score issuer)
+            if (++stage == kStages) { stage = 0; ph ^= 1u; }
           for (int i = 0; i < ntiles; ++i, ++g) {
             const int pb = g & 1;
             if (!wait_phase(bar(PF0 + pb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
@@ -346,7 +386,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO, tQ = tmem + lane_off + kTmQ;
+    const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO;
     const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
     const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
     const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE), peer), r_pf = mapa(bar(PF0), peer);
@@ -355,31 +395,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 
     if (warp < 3 + kAWarps) {
       // -------------------------------------------------------- A: score readers
-      // Per page: read the peer's 32 tokens of this CTA's partial scores, send
-      // them (log2 units, fp16) into the peer's shared memory, zero slack rows,
-      // and stage the query of the next range.
+      // Per page: read the peer's 32 tokens of this CTA's partial scores and send
+      // them (log2 units, fp16) into the peer's shared memory.
       const int atid = threadIdx.x - 96;  // 0 .. 127
-      // the range's latent query half, columns [0, 64) of tensor memory Q (the
-      // helper softmax group stores [64, 128)); one batch of 16 loads per thread
-      auto load_qc = [&](int it) {
-        const int b = plan.item_seq[it];
-        const size_t qrow = ((size_t)b * n_q + j) * H + row;
-        const uint4* src = reinterpret_cast<const uint4*>(q_abs + qrow * kRow + 256 * rank);
-        uint32_t r0[32], r1[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 w0 = row < H ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-          const uint4 w1 = row < H ? __ldg(src + 8 + v) : make_uint4(0, 0, 0, 0);
-          r0[4 * v] = w0.x; r0[4 * v + 1] = w0.y; r0[4 * v + 2] = w0.z; r0[4 * v + 3] = w0.w;
-          r1[4 * v] = w1.x; r1[4 * v + 1] = w1.y; r1[4 * v + 2] = w1.z; r1[4 * v + 3] = w1.w;
-        }
-        tmem_st32(tQ, r0);
-        tmem_st32(tQ + 32, r1);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(QCF));
-      };
-      if (it0 < it1) load_qc(it0);
       int g = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
@@ -408,8 +426,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             w.w = cvt_f16x2(__uint_as_float(r[8 * q8 + 6]) * sl2, __uint_as_float(r[8 * q8 + 7]) * sl2);
             st_async_v4(xa + q8 * 128 * 16, w, xf);
           }
-          // every score MMA of this range is done: stage the next range's query
-          if (i == ntiles - 1 && it + 1 < it1) load_qc(it + 1);
         }
       }
     } else {
@@ -429,28 +445,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       float l_g = 0.f, m_l = -INFINITY;  // this group's sum over the range so far, on reference m_l
       int g = 0, lg_n = 0, iv_n = 0;
       bool ok = true;
-      // The group that does not handle a range's last page helps at the range
-      // switch: it stores columns [64, 128) of the next range's query half
-      // (issuing the loads before the last score MMA completes) and drains
-      // columns [128, 256) of O once the other group has posted 1/l.
-      auto q_loads = [&](int it, uint32_t (&r0)[32], uint32_t (&r1)[32]) {
-        const size_t qrow = ((size_t)plan.item_seq[it] * n_q + j) * H + row;
-        const uint4* src = reinterpret_cast<const uint4*>(q_abs + qrow * kRow + 256 * rank + 128);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 w0 = row < H ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
-          const uint4 w1 = row < H ? __ldg(src + 8 + v) : make_uint4(0, 0, 0, 0);
-          r0[4 * v] = w0.x; r0[4 * v + 1] = w0.y; r0[4 * v + 2] = w0.z; r0[4 * v + 3] = w0.w;
-          r1[4 * v] = w1.x; r1[4 * v + 1] = w1.y; r1[4 * v + 2] = w1.z; r1[4 * v + 3] = w1.w;
-        }
-      };
-      auto q_store = [&](const uint32_t (&r0)[32], const uint32_t (&r1)[32]) {
-        tmem_st32(tQ + 64, r0);
-        tmem_st32(tQ + 96, r1);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(QCF));
-      };
+      // The group that does not handle a range's last page drains columns
+      // [128, 256) of O at the range switch, once the other group has posted 1/l.
       // O columns [128 h, 128 h + 128) of this CTA's half, scaled by inv, into the
       // head-minor partials o_part[item][j][column / 4][head][column % 4]
       auto drain_o = [&](int it, int half, float inv) {
@@ -470,11 +466,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           }
         }
       };
-      if (grp == 1 && it0 < it1) {
-        uint32_t r0[32], r1[32];
-        q_loads(it0, r0, r1);
-        q_store(r0, r1);
-      }
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
         const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
@@ -486,16 +477,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           if ((g & 1) != grp) {
             if (i == ntiles - 1) {
               // helper at the end of the range handled by the other group
-              if (it + 1 < it1) {
-                uint32_t r0[32], r1[32];
-                q_loads(it + 1, r0, r1);
-                // the range's last score MMA has read tensor-memory Q (the other
-                // group's barrier: its previous phase, page g-2, completed before
-                // the other group posted the reference maximum of page g-2)
-                if (!wait_phase(bar(SF0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
-                tc_fence_after();
-                q_store(r0, r1);
-              }
               if (!wait_phase(bar(IVF0 + grp), iv_n & 1, abort_flag, err_word)) { ok = false; break; }
               ++iv_n;
               float inv;
@@ -561,7 +542,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             // slack rows past the context may hold any bits: zero this CTA's latent
             // half so 0-weight x NaN cannot reach O. The score MMAs have read the
             // stage (SF); the value MMAs read it after this group's P-ready arrive.
-            const int stage = g % kStages;
+            const int stage = (g + kQSlots * (li + 1)) % kStages;  // ring slot of page g
             const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
             const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
             for (int z = gtid; z < nz; z += kGThreads) {
@@ -736,14 +717,15 @@ int decode_max_workers() {
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
                           int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s) {
-  CUtensorMap map_c, map_kr, map_qkr;
+  CUtensorMap map_c, map_kr, map_qkr, map_q;
   const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
   const uint64_t q_dims[2] = {kRow, (uint64_t)B * n_q * H};
   const uint64_t row_stride[1] = {kRow * 2};
-  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 128};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 128}, box_q[2] = {64, 128};
   if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
       !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64) ||
-      !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64))
+      !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64) ||
+      !make_tmap(&map_q, q_abs, 2, q_dims, row_stride, box_q, 128))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -754,7 +736,7 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
   }
   const float sl2 = scale * 1.4426950408889634f;
   dim3 grid(2 * G, n_q, 1);
-  return launch_pdl(decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, q_abs,
+  return launch_pdl(decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, map_q,
                     block_table, n_q, H, max_pages, num_pages, sl2, plan, err_word);
 }
 
