@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 #define MLA_MAX_BATCH 4096
 
 typedef enum {
@@ -52,7 +52,8 @@ typedef enum {
     MLA_ERR_WORKSPACE_TOO_SMALL = 3,
     MLA_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
     MLA_ERR_TIMEOUT = 5,           /* device: a bounded wait gave up */
-    MLA_ERR_BOUNDS = 6             /* device: seq_len or page id out of range */
+    MLA_ERR_BOUNDS = 6,            /* device: seq_len or page id out of range */
+    MLA_ERR_RANGE = 7              /* device: a split partial outside the fp16 range */
 } mla_status;
 
 /* Human-readable name of a status code. Never NULL. */
@@ -108,9 +109,12 @@ mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const ui
  *   seq_len_eff[B]          the context lengths actually used (clamped)
  *   item_seq[I], item_page0[I], item_page1[I]   sequence and page range
  *   lse_part[I][n_q][H]     float, natural-log sum-exp of the range's scores
- *   o_part[I][n_q][128][H][4] float, the range's softmax-normalised sum of
- *                           latents, head-minor in groups of four columns:
- *                           o_part[k][j][c / 4][h][c % 4] is column c of head h
+ *   o_part[I][n_q][64][H][8] fp16, the range's softmax-normalised sum of
+ *                           latents, head-minor in groups of eight columns:
+ *                           o_part[k][j][c / 8][h][c % 8] is column c of head h.
+ *                           A normalised partial is a convex combination of
+ *                           cached latents, so |value| <= max |c|; values beyond
+ *                           the fp16 range (65504) are reported as MLA_ERR_RANGE.
  */
 int mla_decode_default_splits(int n_q);
 size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);

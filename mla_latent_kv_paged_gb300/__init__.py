@@ -35,6 +35,7 @@ STATUS = {
     4: "MLA_ERR_CUDA",
     5: "MLA_ERR_TIMEOUT",
     6: "MLA_ERR_BOUNDS",
+    7: "MLA_ERR_RANGE",
 }
 
 EXPORTS = [

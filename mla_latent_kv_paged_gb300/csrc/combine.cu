@@ -3,9 +3,10 @@
 // decode technique):
 //   lse = ln sum_k exp(lse_k),   u = sum_k exp(lse_k - lse) * o_k
 // One block per (sequence, query) row and 32-column slice, two threads per
-// head (16 columns each); the loads of four partials are in flight together. The partials are head-minor in groups of four columns
-// (o_part[k][j][column / 4][head][column % 4]), so a warp reads 32
-// consecutive heads of four columns as one 512-byte run; the bf16 result goes
+// head (16 columns each); the loads of four partials are in flight together.
+// The partials are fp16, head-minor in groups of eight columns
+// (o_part[k][j][column / 8][head][column % 8]), so a warp reads 32
+// consecutive heads of eight columns as one 512-byte run; the bf16 result goes
 // through shared memory so the stores of u are row-contiguous.
 #include "mla_internal.cuh"
 
@@ -45,26 +46,29 @@ combine_kernel(Plan plan, int n_q, int H, uint16_t* __restrict__ u, float* __res
     if (m != -INFINITY) {
       for (int kb = k0; kb < k1; kb += kKB) {
         float w[kKB];
-        float4 v[kKB][4];
+        uint4 v[kKB][2];
 #pragma unroll
         for (int i = 0; i < kKB; ++i) {
           const int k = kb + i;
           const float lk = k < k1 ? lse_of(k) : -INFINITY;
           w[i] = lk == -INFINITY ? 0.f : expf(lk - m);
-          const float4* src = reinterpret_cast<const float4*>(plan.o_part) +
-                              (((size_t)min(k, k1 - 1) * n_q + j) * (kDC / 4) + c0 / 4) * H + h;
+          const uint4* src = reinterpret_cast<const uint4*>(plan.o_part) +
+                             (((size_t)min(k, k1 - 1) * n_q + j) * (kDC / 8) + c0 / 8) * H + h;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[i][q] = k < k1 ? src[(size_t)q * H] : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < 2; ++q) v[i][q] = k < k1 ? src[(size_t)q * H] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < kKB; ++i) {
           wsum += w[i];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[4 * q] = fmaf(w[i], v[i][q].x, acc[4 * q]);
-            acc[4 * q + 1] = fmaf(w[i], v[i][q].y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(w[i], v[i][q].z, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(w[i], v[i][q].w, acc[4 * q + 3]);
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t ww[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = sm100::f16x2_to_f32(ww[e]);
+              acc[8 * q + 2 * e] = fmaf(w[i], f.x, acc[8 * q + 2 * e]);
+              acc[8 * q + 2 * e + 1] = fmaf(w[i], f.y, acc[8 * q + 2 * e + 1]);
+            }
           }
         }
       }

@@ -447,24 +447,33 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       bool ok = true;
       // The group that does not handle a range's last page drains columns
       // [128, 256) of O at the range switch, once the other group has posted 1/l.
-      // O columns [128 h, 128 h + 128) of this CTA's half, scaled by inv, into the
-      // head-minor partials o_part[item][j][column / 4][head][column % 4]
+      // O columns [128 half, 128 half + 128) of this CTA's half, scaled by inv,
+      // as fp16 into the head-minor partials o_part[item][j][column / 8][head][column % 8]
+      // (each warp store is 512 contiguous bytes).
       auto drain_o = [&](int it, int half, float inv) {
-        float4* dst = reinterpret_cast<float4*>(plan.o_part) +
-                      ((size_t)(it * n_q + j) * (kDC / 4) + (256 * rank + 128 * half) / 4) * H + row;
+        uint4* dst = reinterpret_cast<uint4*>(plan.o_part) +
+                     ((size_t)(it * n_q + j) * (kDC / 8) + (256 * rank + 128 * half) / 8) * H + row;
+        float amax = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(tO + 128 * half + 32 * c, r);
           tmem_wait_ld();
-          if (row < H) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[(size_t)(8 * c + v) * H] =
-                  make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                              __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              f[e] = __uint_as_float(r[8 * v + e]) * inv;
+              amax = fmaxf(amax, fabsf(f[e]));
+            }
+            if (row < H)
+              dst[(size_t)(4 * c + v) * H] = make_uint4(cvt_f16x2(f[0], f[1]), cvt_f16x2(f[2], f[3]),
+                                                       cvt_f16x2(f[4], f[5]), cvt_f16x2(f[6], f[7]));
           }
         }
+        // a partial beyond the fp16 range would turn into infinity
+        if (row < H && !(amax <= 65504.f)) report_error(err_word, MLA_ERR_RANGE);
       };
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;

@@ -34,6 +34,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
     case MLA_ERR_BOUNDS: return "MLA_ERR_BOUNDS";
+    case MLA_ERR_RANGE: return "MLA_ERR_RANGE";
     default: return "MLA_ERR_UNKNOWN";
   }
 }

@@ -30,7 +30,7 @@ struct Plan {
   int32_t* item_page0;   // [I]
   int32_t* item_page1;   // [I]
   float* lse_part;       // [I][n_q][H]
-  float* o_part;         // [I][n_q][H][512]
+  uint16_t* o_part;      // [I][n_q][64][H][8] fp16, head-minor
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -52,7 +52,7 @@ __host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H,
   size_t o_p0 = take(I * 4);
   size_t o_p1 = take(I * 4);
   size_t o_lse = take(I * n_q * H * 4);
-  size_t o_o = take(I * n_q * H * (size_t)kDC * 4);
+  size_t o_o = take(I * n_q * H * (size_t)kDC * 2);
   if (base && p) {
     char* c = reinterpret_cast<char*>(base);
     p->hdr = reinterpret_cast<int32_t*>(c + o_hdr);
@@ -63,7 +63,7 @@ __host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H,
     p->item_page0 = reinterpret_cast<int32_t*>(c + o_p0);
     p->item_page1 = reinterpret_cast<int32_t*>(c + o_p1);
     p->lse_part = reinterpret_cast<float*>(c + o_lse);
-    p->o_part = reinterpret_cast<float*>(c + o_o);
+    p->o_part = reinterpret_cast<uint16_t*>(c + o_o);
   }
   return off;
 }

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     for name in decl:
         assert hasattr(lib, name), name
     assert set(mla.EXPORTS) <= set(decl)
-    assert lib.mla_abi_version() == 2
+    assert lib.mla_abi_version() == 3
 
 
 def test_status_strings(lib):

@@ -87,20 +87,20 @@ def test_combine_alone_merges_oracle_partials(mla):
     I = G + inp.B
     offs, off = [], 0
     for nbytes in [64 * 4, (G + 1) * 4, (inp.B + 1) * 4, inp.B * 4, I * 4, I * 4, I * 4,
-                   I * inp.n_q * inp.H * 4, I * inp.n_q * inp.H * 512 * 4]:
+                   I * inp.n_q * inp.H * 4, I * inp.n_q * inp.H * 512 * 2]:
         offs.append(off)
         off = (off + nbytes + 255) // 256 * 256
     host = np.zeros(ws.numel(), dtype=np.uint8)
     host[offs[2]:offs[2] + (inp.B + 1) * 4] = pl["seq_item"].astype(np.int32).view(np.uint8)
     lse_part = np.full((I, inp.n_q, inp.H), -np.inf, dtype=np.float32)
-    o_part = np.zeros((I, inp.n_q, 128, inp.H, 4), dtype=np.float32)  # [c/4][h][c%4]
+    o_part = np.zeros((I, inp.n_q, 64, inp.H, 8), dtype=np.float16)  # [c/8][h][c%8]
     rows = np.arange(inp.B * inp.n_q * inp.H)
     for k, (b, p0, p1) in enumerate(pl["items"]):
         part = oracle.split_partials_f64(inp, [[p0 * 64, p1 * 64]], rows)
         for j in range(inp.n_q):
             r = (b * inp.n_q + j) * inp.H + np.arange(inp.H)
             lse_part[k, j] = part["lse"][r, 0]
-            o_part[k, j] = part["u"][r, 0].reshape(inp.H, 128, 4).transpose(1, 0, 2)
+            o_part[k, j] = part["u"][r, 0].reshape(inp.H, 64, 8).transpose(1, 0, 2)
     host[offs[7]:offs[7] + lse_part.nbytes] = lse_part.view(np.uint8).ravel()
     host[offs[8]:offs[8] + o_part.nbytes] = o_part.view(np.uint8).ravel()
     ws.copy_(torch.from_numpy(host))
@@ -231,6 +231,15 @@ def test_device_errors_are_reported_without_faulting(mla):
                     n_q=1, err_word=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 6
+    # latents beyond the fp16 range of the split partials (|c| = 2^17): the
+    # normalised partial of a range is a convex combination of them
+    err.zero_()
+    big = d["cache"].clone()
+    big[..., :512] = 131072.0
+    mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], big, d["block_table"], d["seq_lens"],
+                    n_q=1, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 7
     # the context still works afterwards
     r = run_step(mla, inp, pg)
     assert r["err"] == 0
