@@ -80,7 +80,7 @@ def test_cache_size_numbers_from_the_pages(lib):
 
 def test_workspace_size_query(lib):
     n = lib.mla_decode_workspace_bytes(32, 1, 128, 76)
-    assert n >= (76 + 32) * 128 * 512 * 4
+    assert n >= (76 + 32) * 128 * 512 * 2  # fp16 partials
     assert lib.mla_decode_workspace_bytes(0, 1, 128, 76) == 0
     assert lib.mla_decode_workspace_bytes(32, 3, 128, 76) == 0
     assert lib.mla_decode_workspace_bytes(32, 1, 129, 76) == 0
