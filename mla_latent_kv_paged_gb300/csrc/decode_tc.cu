@@ -32,12 +32,13 @@
 // this CTA's P half for two pages [320,352), the CTA's latent half of q_abs as
 // the score MMAs' A operand [384,512). Shared memory: 5-slot ring (180 KB) of
 // page halves and, at the start of each range, the latent query half (TMA into
-// two slots, then tcgen05.cp into tensor memory), the positional half of q_abs
+// two slots; the score readers move it into tensor memory), the positional half of q_abs
 // (2 x 8 KB), the peer's partial scores (8 KB), the peer's P half (2 x 8 KB),
 // the exchange vectors.
 //
 // Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
-// value-MMA issuer, 3..6 = score readers (the peer's tokens of S), 7..14 =
+// value-MMA issuer, 3..6 = score readers (the peer's tokens of S, the query
+// stage-in from the ring into tensor memory), 7..14 =
 // softmax and epilogue in two groups of four warps that take alternate pages
 // (one thread per head row, the CTA's 32 tokens of the page). The score MMAs
 // of page g+1 run while the softmax of page g is in flight; the value MMAs
@@ -85,8 +86,8 @@ constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 // parity wait is only sound if the barrier's previous phase is one this
 // waiter has already seen complete.
 enum {
-  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QDONE = QKRE0 + 2,
-  SF0 = QDONE + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
+  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
+  SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
   MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
   MMAD = OFREE + 1,
   kNumBars = MMAD + 1
@@ -142,7 +143,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     mbar_init(bar(SFREE), kAThreads + kGThreads);
     mbar_init(bar(XE), 1);   // armed here, completed by the peer's four 4-byte tokens
     mbar_init(bar(MRF), kGThreads);  // the reference maximum of a page posted
-    mbar_init(bar(QDONE), 1);  // every score MMA of a range done: tensor-memory Q may be replaced
+    mbar_init(bar(QCF), kAThreads);  // the range's latent query half is in tensor memory
     mbar_init(bar(OFREE), 2 * kGThreads);        // both halves of O drained
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
@@ -304,22 +305,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0, qb = li & 1;
           const int ntiles = plan.item_page1[it] - plan.item_page0[it];
-          // the range's query: the latent half from its two ring slots into
-          // tensor memory (once every score MMA of the previous range is done),
+          // the range's query: the score readers have moved the latent half from
+          // its two ring slots into tensor memory (and read the slots: free them);
           // the positional half stays in shared memory
-          if (li > 0 && !wait_phase(bar(QDONE), (li - 1) & 1, abort_flag, err_word)) { ok = false; break; }
-          for (int q = 0; q < kQSlots && ok; ++q) {
-            if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sq = sbase + kOffStage + stage * kStageBytes;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)  // 16 bf16 (32 bytes) of each row per copy
-              tmem_cp_128x256b(tmem + kTmQ + 64 * q + 8 * k,
-                               dQK_c + da(sq + (k >> 2) * kQBoxBytes + (k & 3) * 32));
-            mma_commit(bar(EMPTY0 + stage));  // the slot is free once the copies are done
+          if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word) ||
+              !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          for (int q = 0; q < kQSlots; ++q) {
+            mbar_arrive(bar(EMPTY0 + stage));
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
-          if (!ok || !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           for (int i = 0; i < ntiles; ++i, ++g) {
             if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
                 !wait_phase(bar(SFREE), (g & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
@@ -335,10 +329,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             mma_ss(d, ar, br, kIdQK, 1u);
             mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
             mma_commit(bar(SF0 + (g & 1)));
-            if (i == ntiles - 1) {
-              mma_commit(bar(QKRE0 + qb));
-              mma_commit(bar(QDONE));
-            }
+            if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
         }
@@ -398,10 +389,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       // Per page: read the peer's 32 tokens of this CTA's partial scores and send
       // them (log2 units, fp16) into the peer's shared memory.
       const int atid = threadIdx.x - 96;  // 0 .. 127
+      const uint32_t tQ = tmem + lane_off + kTmQ;
       int g = 0;
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
+        const int li = it - it0;
         const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+        // the range's latent query half: this thread's head row from the two ring
+        // slots (four [128][64] boxes, 128B-swizzled: 16-byte chunk c of row r at
+        // c ^ (r % 8)) into tensor memory. The previous range's score MMAs are done
+        // (this warp read the S of its last page), so Q may be overwritten.
+        for (int q = 0; q < kQSlots && ok; ++q) {
+          const int slot = g + kQSlots * li + q;
+          if (!wait_phase(bar(FULL0 + slot % kStages), (slot / kStages) & 1, abort_flag, err_word)) { ok = false; break; }
+          const uint32_t sq = sbase + kOffStage + (slot % kStages) * kStageBytes + (uint32_t)row * 128;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(r[4 * c]), "=r"(r[4 * c + 1]), "=r"(r[4 * c + 2]), "=r"(r[4 * c + 3])
+                           : "r"(sq + m * kQBoxBytes + ((c ^ (row & 7)) * 16)));
+            tmem_st32(tQ + 64 * q + 32 * m, r);
+          }
+        }
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(QCF));
         for (int i = 0; i < ntiles; ++i, ++g) {
           if (!wait_phase(bar(SF0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
