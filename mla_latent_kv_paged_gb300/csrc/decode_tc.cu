@@ -29,12 +29,12 @@
 // value MMAs (P x C[64][256]).
 //
 // Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S [256,320),
-// this CTA's P half for two pages [320,352), the CTA's latent half of q_abs as
-// the score MMAs' A operand [384,512). Shared memory: 5-slot ring (180 KB) of
-// page halves and, at the start of each range, the latent query half (TMA into
-// two slots; the score readers move it into tensor memory), the positional half of q_abs
-// (2 x 8 KB), the peer's partial scores (8 KB), the peer's P half (2 x 8 KB),
-// the exchange vectors.
+// this CTA's P half for two pages [320,352), the CTA's positional query half
+// [352,368) and latent query half [384,512), the A operands of the score MMAs.
+// Shared memory: 5-slot ring (180 KB) of page halves and, at the start of each
+// range, the query half (TMA into two slots; the score readers move it into
+// tensor memory), the peer's partial scores (one 8 KB
+// buffer per softmax group), the peer's P half (3 x 8 KB), the exchange vectors.
 //
 // Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
 // value-MMA issuer, 3..6 = score readers (the peer's tokens of S, the query
@@ -60,21 +60,21 @@ constexpr int kThreads = 96 + kAThreads + kBThreads;
 constexpr uint32_t kCBoxBytes = 64 * 128;   // [64 tokens][64 latent cols] bf16, 128B swizzle
 constexpr uint32_t kKrBoxBytes = 64 * 64;   // [64 tokens][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
-constexpr uint32_t kQkrBytes = 128 * 64;    // [128 heads][32] bf16, 64B swizzle
+constexpr uint32_t kQrBoxBytes = 64 * 64;   // [64 heads][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kQBoxBytes = 128 * 128;  // [128 heads][64 latent cols] bf16, 128B swizzle
 constexpr int kQSlots = 2;                  // ring slots taken by a range's latent query half (4 boxes)
-constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of 8 tokens][128 heads] fp16
+constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of 8 tokens][128 heads] fp16  // + the peer's partial-score maximum per head (fp32)
 constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads][32 tokens] bf16, 64B swizzle
 constexpr uint32_t kPHalfBytes = kPPeerBytes;
+constexpr int kPBufs = 3;  // P buffers: page g uses g % 3, so its writers wait for page g - 3
 constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
 constexpr uint32_t kTokBytes = 4 * 4;       // "partial consumed" tokens: one per warp of a group
 
 constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffQkr = kOffStage + kStages * kStageBytes;
-constexpr uint32_t kOffX = kOffQkr + 2 * kQkrBytes;   // peer partial scores (one page)
-constexpr uint32_t kOffP = kOffX + kXBytes;            // the peer's half of P, two pages
-constexpr uint32_t kOffMX = kOffP + 2 * kPPeerBytes;   // peer page maxima [2 pages][128]
-constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;    // peer softmax sums [2 ranges][128]
+constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;  // peer partial scores, one buffer per group
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;        // the peer's half of P, two pages
+constexpr uint32_t kOffMX = kOffP + kPBufs * kPPeerBytes;  // peer page maxima [2 groups][128]
+constexpr uint32_t kOffLX = kOffMX + 2 * kVecBytes;  // peer softmax sums [2 ranges][128]
 constexpr uint32_t kOffMR = kOffLX + 2 * kVecBytes;    // reference maximum after the latest page [128]
 constexpr uint32_t kOffLG = kOffMR + kVecBytes;        // handed-over group sums [2 ranges][sum, ref][128]
 constexpr uint32_t kOffIV = kOffLG + 4 * kVecBytes;    // 1 / softmax sum of the range [128]
@@ -86,19 +86,20 @@ constexpr uint32_t kOffBar = kOffTok + kTokBytes;
 // parity wait is only sound if the barrier's previous phase is one this
 // waiter has already seen complete.
 enum {
-  FULL0 = 0, EMPTY0 = FULL0 + kStages, QKRF0 = EMPTY0 + kStages, QKRE0 = QKRF0 + 2, QCF = QKRE0 + 2,
-  SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + 2, XF0 = PVD0 + 2, XE = XF0 + 2,
-  MXF0 = XE + 1, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
+  FULL0 = 0, EMPTY0 = FULL0 + kStages, QCF = EMPTY0 + kStages,
+  SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + kPBufs, XF0 = PVD0 + kPBufs, XE0 = XF0 + 2,
+  MXF0 = XE0 + 2, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
   MMAD = OFREE + 1,
   kNumBars = MMAD + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffSlots + 16;  // the base is checked to be 1024-byte aligned
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(2 * kQBoxBytes + kQrBoxBytes <= kStageBytes, "a ring slot holds a query quarter");
 
 // tensor memory columns: O[128][256] fp32, S[128][64] fp32, this CTA's half of P
 // (bf16 pairs) for two pages, the CTA's latent half of q_abs (bf16 pairs)
-constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQ = 384, kTmCols = 512;
+constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQr = 368, kTmQ = 384, kTmCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
 
@@ -127,34 +128,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       mbar_init(bar(EMPTY0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(QKRF0 + i), 1);
-      mbar_init(bar(QKRE0 + i), 1);
-      mbar_init(bar(PF0 + i), kGThreads + 1);  // the group's rows + the arming arrive for the peer's half
-      mbar_init(bar(PVD0 + i), 2);   // the value MMAs of this page done in both CTAs
-      mbar_init(bar(MXF0 + i), 1);
       mbar_init(bar(LXF0 + i), 1);
       mbar_init(bar(LGF0 + i), kGThreads);  // a group's sums handed over
       mbar_init(bar(IVF0 + i), kGThreads);  // 1/l posted for helper group i
     }
+    for (int i = 0; i < kPBufs; ++i) {
+      mbar_init(bar(PF0 + i), kGThreads + 1);  // a group's rows + the arming arrive for the peer's half
+      mbar_init(bar(PVD0 + i), 2);             // the value MMAs of the page done in both CTAs
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SF0 + i), 1);
       mbar_init(bar(XF0 + i), 1);  // armed here, filled by the peer's st.async
+      mbar_init(bar(XE0 + i), 1);  // armed here, completed by the peer's four 4-byte tokens
+      mbar_init(bar(MXF0 + i), 1);
     }
     mbar_init(bar(SFREE), kAThreads + kGThreads);
-    mbar_init(bar(XE), 1);   // armed here, completed by the peer's four 4-byte tokens
+
     mbar_init(bar(MRF), kGThreads);  // the reference maximum of a page posted
     mbar_init(bar(QCF), kAThreads);  // the range's latent query half is in tensor memory
     mbar_init(bar(OFREE), 2 * kGThreads);        // both halves of O drained
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
     *abort_flag = 0;
     fence_mbar_init();
+    for (int i = 0; i < kPBufs; ++i) mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
     for (int i = 0; i < 2; ++i) {
-      mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
-      mbar_arrive_expect_tx(bar(MXF0 + i), kVecBytes);
       mbar_arrive_expect_tx(bar(LXF0 + i), kVecBytes);
       mbar_arrive_expect_tx(bar(XF0 + i), kXBytes);
+      mbar_arrive_expect_tx(bar(XE0 + i), kTokBytes);
+      mbar_arrive_expect_tx(bar(MXF0 + i), kVecBytes);
     }
-    mbar_arrive_expect_tx(bar(XE), kTokBytes);
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_c);
@@ -183,7 +185,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const uint64_t pol_keep = policy_evict_last();
     int stage = 0;
     uint32_t ph = 0;
-    int last_ph[kStages], last_qph[2] = {-1, -1};
+    int last_ph[kStages];
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
     bool ok = true;
@@ -218,27 +220,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     Cursor ld;
     cur_init(ld, it0);
     while (ok && ld.it < it1) {
-      const int it = ld.it, li = it - it0, qb = li & 1;
+      const int it = ld.it;
       if (ld.pg == plan.item_page0[it]) {
-        // first page of a range: its positional query half
-        if (!wait_phase(bar(QKRE0 + qb), ((li >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(QKRF0 + qb), kQkrBytes);
-          tma_load_2d(sbase + kOffQkr + qb * kQkrBytes, &map_qkr, bar(QKRF0 + qb), kDC + 32 * (int)rank,
-                      (plan.item_seq[it] * n_q + j) * H, pol_keep);
-        }
-        last_qph[qb] = (li >> 1) & 1;
-        // and its latent half, four [128 heads][64] boxes into the next two ring
-        // slots; the score-MMA issuer copies them into tensor memory
+        // first page of a range: the CTA's half of its query into the next two
+        // ring slots (the score readers move it into tensor memory). Slot q holds
+        // latent boxes [128 heads][64] for columns 256r + 128q + {0, 64} and, in
+        // its last 4 KB, positional rows [64q, 64q + 64) of columns 512 + 32r.
         const int qrow = (plan.item_seq[it] * n_q + j) * H;
         for (int q = 0; q < kQSlots && ok; ++q) {
           if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
           if (lane == 0) {
             const uint32_t fb = bar(FULL0 + stage);
             const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
-            mbar_arrive_expect_tx(fb, 2 * kQBoxBytes);
+            mbar_arrive_expect_tx(fb, 2 * kQBoxBytes + kQrBoxBytes);
             for (int m = 0; m < 2; ++m)
               tma_load_2d(dst + m * kQBoxBytes, &map_q, fb, 256 * (int)rank + 128 * q + 64 * m, qrow, pol_keep);
+            tma_load_2d(dst + 2 * kQBoxBytes, &map_qkr, fb, kDC + 32 * (int)rank, qrow + 64 * q, pol_keep);
           }
           last_ph[stage] = (int)ph;
           __syncwarp();
@@ -267,12 +264,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     if (!ok) {
       // let every issued copy land before this CTA can exit
 #pragma unroll
-      for (int i = 0; i < kStages + 2; ++i) {
-        const int ph_i = i < kStages ? last_ph[i] : last_qph[i - kStages];
-        const uint32_t b_i = i < kStages ? bar(FULL0 + i) : bar(QKRF0 + i - kStages);
-        if (ph_i >= 0) {
+      for (int i = 0; i < kStages; ++i) {
+        if (last_ph[i] >= 0) {
           const long long t0 = clock64();
-          while (!mbar_try_wait(b_i, (uint32_t)ph_i) && clock64() - t0 < kWaitLimitCycles) {
+          while (!mbar_try_wait(bar(FULL0 + i), (uint32_t)last_ph[i]) && clock64() - t0 < kWaitLimitCycles) {
           }
         }
       }
@@ -303,13 +298,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       if (warp == 1) {
         // ---- score MMAs: S = q_abs half . [c ; k^R] half of the page
         for (int it = it0; it < it1 && ok; ++it) {
-          const int li = it - it0, qb = li & 1;
+          const int li = it - it0;
           const int ntiles = plan.item_page1[it] - plan.item_page0[it];
           // the range's query: the score readers have moved the latent half from
           // its two ring slots into tensor memory (and read the slots: free them);
           // the positional half stays in shared memory
-          if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word) ||
-              !wait_phase(bar(QKRF0 + qb), (li >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+          if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word)) { ok = false; break; }
           for (int q = 0; q < kQSlots; ++q) {
             mbar_arrive(bar(EMPTY0 + stage));
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
@@ -324,12 +318,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             for (int ks = 0; ks < 16; ++ks)
               mma_ts(d, tmem + kTmQ + ks * 8, bc + (((ks >> 2) * kCBoxBytes + (ks & 3) * 32) >> 4), kIdQK,
                      ks > 0 ? 1u : 0u);
-            const uint64_t ar = dQK_r + da(sbase + kOffQkr + qb * kQkrBytes);
+            // positional part: A = the positional query half in tensor memory
             const uint64_t br = dQK_r + da(sbase + kOffStage + stage * kStageBytes + 4 * kCBoxBytes);
-            mma_ss(d, ar, br, kIdQK, 1u);
-            mma_ss(d, ar + 2, br + 2, kIdQK, 1u);
+            mma_ts(d, tmem + kTmQr, br, kIdQK, 1u);
+            mma_ts(d, tmem + kTmQr + 8, br + 2, kIdQK, 1u);
             mma_commit(bar(SF0 + (g & 1)));
-            if (i == ntiles - 1) mma_commit(bar(QKRE0 + qb));
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
         }
@@ -342,8 +335,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           for (int q = 0; q < kQSlots; ++q)  // the range's query slots (released by the score issuer)
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           for (int i = 0; i < ntiles; ++i, ++g) {
-            const int pb = g & 1;
-            if (!wait_phase(bar(PF0 + pb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            const int pb = g % kPBufs;
+            if (!wait_phase(bar(PF0 + pb), (g / kPBufs) & 1, abort_flag, err_word)) { ok = false; break; }
             // the first value MMA of a range overwrites O: the previous range's
             // epilogue must have read it
             if (i == 0 && li > 0 && !wait_phase(bar(OFREE), (li - 1) & 1, abort_flag, err_word)) { ok = false; break; }
@@ -379,9 +372,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + kTmS, tO = tmem + lane_off + kTmO;
     const uint32_t r_x = mapa(sbase + kOffX, peer), r_p = mapa(sbase + kOffP, peer);
-    const uint32_t r_mx = mapa(sbase + kOffMX, peer), r_lx = mapa(sbase + kOffLX, peer);
-    const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE), peer), r_pf = mapa(bar(PF0), peer);
-    const uint32_t r_mxf = mapa(bar(MXF0), peer), r_lxf = mapa(bar(LXF0), peer);
+    const uint32_t r_lx = mapa(sbase + kOffLX, peer), r_mx = mapa(sbase + kOffMX, peer);
+    const uint32_t r_xf = mapa(bar(XF0), peer), r_xe = mapa(bar(XE0), peer), r_pf = mapa(bar(PF0), peer);
+    const uint32_t r_lxf = mapa(bar(LXF0), peer), r_mxf = mapa(bar(MXF0), peer);
     const uint32_t r_tok = mapa(sbase + kOffTok, peer);
 
     if (warp < 3 + kAWarps) {
@@ -413,6 +406,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
                            : "r"(sq + m * kQBoxBytes + ((c ^ (row & 7)) * 16)));
             tmem_st32(tQ + 64 * q + 32 * m, r);
           }
+          if ((row >> 6) == q) {  // this row's positional half: 64 bytes, 64B-swizzled (warp-uniform)
+            const uint32_t sr = sbase + kOffStage + (slot % kStages) * kStageBytes + 2 * kQBoxBytes;
+            const int rl = row & 63;
+            uint32_t r[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(r[4 * c]), "=r"(r[4 * c + 1]), "=r"(r[4 * c + 2]), "=r"(r[4 * c + 3])
+                           : "r"(sr + rl * 64 + ((c ^ ((rl >> 1) & 3)) * 16)));
+            tmem_st16(tmem + lane_off + kTmQr, r);
+          }
         }
         if (!ok) break;
         tmem_wait_st();
@@ -426,12 +430,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(bar(SFREE));
-          // the peer has read this CTA's partial of the previous page
-          if (g >= 1) {
-            if (!wait_phase(bar(XE), (g - 1) & 1, abort_flag, err_word)) { ok = false; break; }
-            if (atid == 0) mbar_arrive_expect_tx(bar(XE), kTokBytes);  // arm for this page
+          // the peer has read this CTA's partial of page g-2 (same buffer)
+          if (g >= 2) {
+            if (!wait_phase(bar(XE0 + (g & 1)), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
+            if (atid == 0) mbar_arrive_expect_tx(bar(XE0 + (g & 1)), kTokBytes);  // arm for this page
           }
-          const uint32_t xa = r_x + (uint32_t)row * 16;
+          const uint32_t xa = r_x + (uint32_t)(g & 1) * kXBytes + (uint32_t)row * 16;
           const uint32_t xf = r_xf + 8u * (uint32_t)(g & 1);
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
@@ -506,7 +510,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
               ++iv_n;
               float inv;
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(inv) : "r"(sbase + kOffIV + vec_off));
-              if (!wait_phase(bar(PVD0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+              if (!wait_phase(bar(PVD0 + g % kPBufs), (g / kPBufs) & 1, abort_flag, err_word)) { ok = false; break; }
               tc_fence_after();
               drain_o(it, 1, inv);
               tc_fence_before();
@@ -516,6 +520,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           }
           const int xb = g & 1;
           // this CTA's partial scores of its 32 tokens
+          const int nv = n_att - ((pg0 + i) * kPage + 32 * (int)rank);  // valid tokens among these 32
           if (!wait_phase(bar(SF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           {
@@ -535,7 +540,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             uint4 w;
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                         : "r"(sbase + kOffX + (uint32_t)((q8 * 128 + row) * 16)));
+                         : "r"(sbase + kOffX + xb * kXBytes + (uint32_t)((q8 * 128 + row) * 16)));
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -547,21 +552,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           __syncwarp();
           // tell the peer this warp has read its partial (a 4-byte token completes
           // the peer's barrier; the loads above have all returned by now)
-          if (lane == 0) st_async_b32(r_tok + (uint32_t)gwarp * 4, 1u, r_xe);
-          const int nv = n_att - ((pg0 + i) * kPage + 32 * (int)rank);  // valid tokens among these 32
+          if (lane == 0) st_async_b32(r_tok + (uint32_t)gwarp * 4, 1u, r_xe + 8u * xb);
           if (nv < 32) {
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj)
               if (jj >= nv) x[jj] = -INFINITY;
           }
-          // both CTAs' value MMAs of page g-2 are done: this group's P buffer is
-          // free, and the peer's page-max slot for this page was read (the peer
-          // reads it before its P-ready arrive of page g-2)
-          if (g >= 2 && !wait_phase(bar(PVD0 + xb), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
-          float m = x[0];
-#pragma unroll
-          for (int jj = 1; jj < 32; ++jj) m = fmaxf(m, x[jj]);
-          st_async_b32(r_mx + xb * kVecBytes + vec_off, __float_as_uint(m), r_mxf + 8u * xb);
+          // both CTAs' value MMAs of page g-3 are done: P buffer g % 3 is free. (Its
+          // previous phase, page g-6, is complete: the value MMAs complete in page
+          // order and this group waited for page g-5 at page g-2.)
+          const int pb = g % kPBufs;
+          if (g >= kPBufs && !wait_phase(bar(PVD0 + pb), ((g / kPBufs) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
           const int rows_valid = L - (pg0 + i) * kPage;
           if (rows_valid < kPage) {
             // slack rows past the context may hold any bits: zero this CTA's latent
@@ -578,9 +579,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             }
             fence_proxy_async_smem();
           }
-          // the peer's page maximum: the exact page maximum, identical in both CTAs
+          float m = x[0];
+#pragma unroll
+          for (int jj = 1; jj < 32; ++jj) m = fmaxf(m, x[jj]);
+          st_async_b32(r_mx + xb * kVecBytes + vec_off, __float_as_uint(m), r_mxf + 8u * xb);
           if (!wait_phase(bar(MXF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
-          if (gtid == 0) mbar_arrive_expect_tx(bar(MXF0 + xb), kVecBytes);  // arm for page g+2
+          if (gtid == 0) mbar_arrive_expect_tx(bar(MXF0 + xb), kVecBytes);
           float m_p;
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m_p) : "r"(sbase + kOffMX + xb * kVecBytes + vec_off));
           const float mt = fmaxf(m, m_p);
@@ -603,7 +607,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           mbar_arrive(bar(MRF));
           if (__any_sync(0xffffffffu, need)) {
             // O must hold every earlier page before it is rescaled
-            if (!wait_phase(bar(PVD0 + (xb ^ 1)), ((g - 1) >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            if (!wait_phase(bar(PVD0 + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
@@ -627,8 +631,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           const float mref = m_new == -INFINITY ? 0.f : m_new;  // all masked so far: every p is 0
           // P: into tensor memory for this CTA's value MMAs and into the peer's
           // shared memory (64B-swizzled, K-major) for its own
-          const uint32_t pr = r_p + xb * kPPeerBytes + (uint32_t)row * 64;
-          const uint32_t pfr = r_pf + 8u * xb;
+          const uint32_t pr = r_p + pb * kPPeerBytes + (uint32_t)row * 64;
+          const uint32_t pfr = r_pf + 8u * pb;
           float lsum0 = 0.f, lsum1 = 0.f;
           uint32_t pw[16];
 #pragma unroll
@@ -639,7 +643,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             lsum0 += bf16_lo(pw[v]);
             lsum1 += bf16_hi(pw[v]);
           }
-          tmem_st16(tmem + lane_off + kTmP + 16 * xb, pw);
+          tmem_st16(tmem + lane_off + kTmP + 16 * pb, pw);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             st_async_v4(pr + (uint32_t)((c ^ ((row >> 1) & 3)) * 16),
@@ -647,7 +651,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           tmem_wait_st();
           l_g += lsum0 + lsum1;
           tc_fence_before();
-          mbar_arrive(bar(PF0 + xb));
+          mbar_arrive(bar(PF0 + pb));
           if (i == ntiles - 2) {
             // the other group handles the last page of the range: hand over this sum
             const uint32_t lg = sbase + kOffLG + (uint32_t)(lg_n & 1) * 2 * kVecBytes;
@@ -678,7 +682,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             // 1/l for the helper group, which drains the other half of O
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffIV + vec_off), "f"(inv) : "memory");
             mbar_arrive(bar(IVF0 + (grp ^ 1)));
-            if (!wait_phase(bar(PVD0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
+            if (!wait_phase(bar(PVD0 + pb), (g / kPBufs) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
             const size_t orow = ((size_t)it * n_q + j) * H + row;
             drain_o(it, 0, inv);
@@ -746,7 +750,7 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
   const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
   const uint64_t q_dims[2] = {kRow, (uint64_t)B * n_q * H};
   const uint64_t row_stride[1] = {kRow * 2};
-  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 128}, box_q[2] = {64, 128};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 64}, box_q[2] = {64, 128};
   if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
       !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64) ||
       !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64) ||
