@@ -255,3 +255,58 @@ def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q
                      stream=stream)
     out = out_proj(u, w_uv, bufs.get("out"), stream)
     return dict(q_abs=q_abs, u=u, lse=lse, out=out, workspace=ws, num_splits=g)
+
+
+class CapturedStep:
+    """A whole decode step (absorb_q -> decode_paged -> combine -> out_proj)
+    captured once in a CUDA graph, for serving loops with fixed shapes.
+
+    The step owns its query, workspace and output buffers; it keeps pointers to
+    the caller's weights, cache, block_table and seq_lens, so changing their
+    contents in place between calls (appending tokens, new pages) is seen by
+    the next replay: the split plan is derived on the device from seq_lens
+    every time. Shapes (batch, max pages per sequence, heads, n_q) and
+    num_splits are fixed at construction. Calling the object copies the new
+    queries in (from host or device tensors, asynchronously) and replays the
+    graph on the current stream; the returned tensors are the step's own
+    buffers, overwritten by the next call.
+    """
+
+    def __init__(self, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
+                 softmax_scale: float = DEFAULT_SCALE, err_word=None):
+        import torch
+        B = block_table.shape[0]
+        H = w_uk.shape[0]
+        T = B * n_q
+        dev = cache.device
+        g = default_splits(n_q) if num_splits is None else num_splits
+        bf = torch.bfloat16
+        self.q_nope = torch.empty((T, H, D_NOPE), dtype=bf, device=dev)
+        self.q_rope = torch.empty((T, H, D_R), dtype=bf, device=dev)
+        self.bufs = dict(q_abs=torch.empty((T, H, D_ROW), dtype=bf, device=dev),
+                         workspace=torch.empty(workspace_bytes(B, n_q, H, g), dtype=torch.uint8, device=dev),
+                         u=torch.empty((T, H, D_C), dtype=bf, device=dev),
+                         lse=torch.empty((T, H), dtype=torch.float32, device=dev),
+                         out=torch.empty((T, H, D_V), dtype=bf, device=dev))
+        self.q_nope.zero_()
+        self.q_rope.zero_()
+        args = (self.q_nope, self.q_rope, w_uk, w_uv, cache, block_table, seq_lens)
+        kw = dict(n_q=n_q, num_splits=g, softmax_scale=softmax_scale, bufs=self.bufs, err_word=err_word)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):  # one eager run: kernel attributes, module loading
+            decode_step(*args, **kw)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            decode_step(*args, **kw)
+        self.num_splits = g
+
+    def __call__(self, q_nope=None, q_rope=None):
+        """q_nope [T,H,128], q_rope [T,H,64] (bf16, host or device); None keeps the previous ones."""
+        if q_nope is not None:
+            self.q_nope.copy_(q_nope, non_blocking=True)
+        if q_rope is not None:
+            self.q_rope.copy_(q_rope, non_blocking=True)
+        self.graph.replay()
+        return dict(q_abs=self.bufs["q_abs"], u=self.bufs["u"], lse=self.bufs["lse"], out=self.bufs["out"])

@@ -76,6 +76,35 @@ def test_out_proj(mla, T, H):
     assert (np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5).all()
 
 
+def test_captured_step_replays_equal_eager_steps(mla):
+    """CapturedStep gives the eager step's bits, and sees in-place changes of seq_lens / block_table."""
+    import torch
+    inp = mi.make_inputs(B=3, H=128, n_q=2, seq_lens=[70, 300, 129], seed=77)
+    pg = mi.make_paged(inp, spare_pages=8)
+    d = device_inputs(inp, pg)
+    step = mla.CapturedStep(d["w_uk"], d["w_uv"], d["cache"], d["block_table"], d["seq_lens"], n_q=2, num_splits=5)
+    r = step(d["q_nope"], d["q_rope"])
+    e = mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], d["block_table"],
+                        d["seq_lens"], n_q=2, num_splits=5)
+    torch.cuda.synchronize()
+    for k in ("u", "out"):
+        assert torch.equal(r[k].view(torch.int16), e[k].view(torch.int16)), k
+    assert torch.equal(r["lse"], e["lse"])
+    compare_full(inp, r)
+    # shorter contexts and another page order, written in place: the replay follows them
+    inp2 = mi.make_inputs(B=3, H=128, n_q=2, seq_lens=[66, 200, 64], seed=78)
+    pg2 = mi.make_paged(inp2, perm_seed=5, spare_pages=8, max_pages=pg.max_pages)
+    d2 = device_inputs(inp2, pg2)
+    d["cache"][: d2["cache"].shape[0]].copy_(d2["cache"])
+    d["w_uk"].copy_(d2["w_uk"])  # the step keeps pointers to the weights as well
+    d["w_uv"].copy_(d2["w_uv"])
+    d["block_table"].copy_(d2["block_table"])
+    d["seq_lens"].copy_(d2["seq_lens"])
+    r2 = step(d2["q_nope"], d2["q_rope"])
+    torch.cuda.synchronize()
+    compare_full(inp2, r2)
+
+
 def test_combine_alone_merges_oracle_partials(mla):
     """Feed oracle partials through the documented workspace layout into mla_combine."""
     import torch
