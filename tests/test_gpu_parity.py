@@ -217,6 +217,29 @@ def test_plan_is_bit_exact(mla):
     assert np.array_equal(i32(offs[6], n), pl["items"][:, 2])
 
 
+@pytest.mark.parametrize("splits", [None, 7000])
+def test_maximum_batch_short_contexts(mla, splits):
+    """B = MLA_MAX_BATCH sequences of 1..130 tokens (one-token contexts included); 7000 splits is
+    more ranges than pages, so some ranges are empty and every other range holds one page."""
+    lens = np.random.default_rng(4096).integers(1, 131, size=4096)
+    lens[:3] = [1, 64, 65]
+    inp = mi.make_inputs(B=4096, H=8, n_q=1, seq_lens=list(lens), seed=4096)
+    pg = mi.make_paged(inp, spare_pages=2)
+    r = run_step(mla, inp, pg, num_splits=splits)
+    assert r["err"] == 0
+    compare_full(inp, r)
+    if splits is not None:
+        G, B = splits, inp.B
+        ws = r["workspace"].cpu().numpy()
+        offs, off = [], 0
+        for nbytes in [64 * 4, (G + 1) * 4, (B + 1) * 4]:
+            offs.append(off)
+            off = (off + nbytes + 255) // 256 * 256
+        pl = plan_mirror(inp.seq_lens, 1, pg.max_pages, G)
+        assert np.array_equal(ws[offs[1]:offs[1] + 4 * (G + 1)].view(np.int32), pl["range_item"])
+        assert np.array_equal(ws[offs[2]:offs[2] + 4 * (B + 1)].view(np.int32), pl["seq_item"])
+
+
 def test_incremental_decode_matches_fresh(mla):
     """Huny section 5 case 5: 8 prefill tokens, then 4 decode steps each appending
     one latent; every step matches the oracle at that length, and decoding a
