@@ -35,8 +35,21 @@ combine_kernel(Plan plan, int n_q, int H, uint16_t* __restrict__ u, float* __res
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
   float m = -INFINITY, wsum = 0.f;
   if (h < H) {
-    // the maximum log-sum-exp, eight independent loads at a time
-    for (int kb = k0; kb < k1; kb += 8) {
+    const uint4* o16 = reinterpret_cast<const uint4*>(plan.o_part);
+    auto src_of = [&](int k) { return o16 + (((size_t)k * n_q + j) * (kDC / 8) + c0 / 8) * H + h; };
+    // the first eight log-sum-exps and the first four pieces' data in flight
+    // together: one dependent round trip when a sequence has at most four pieces
+    float l8[8];
+    uint4 v[kKB][2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l8[i] = k0 + i < k1 ? lse_of(k0 + i) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kKB; ++i)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) v[i][q] = k0 + i < k1 ? src_of(k0 + i)[(size_t)q * H] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, l8[i]);
+    for (int kb = k0 + 8; kb < k1; kb += 8) {  // more than eight pieces
       float l[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) l[i] = kb + i < k1 ? lse_of(kb + i) : -INFINITY;
@@ -46,16 +59,17 @@ combine_kernel(Plan plan, int n_q, int H, uint16_t* __restrict__ u, float* __res
     if (m != -INFINITY) {
       for (int kb = k0; kb < k1; kb += kKB) {
         float w[kKB];
-        uint4 v[kKB][2];
+        if (kb > k0) {  // later batches: their own loads
+#pragma unroll
+          for (int i = 0; i < kKB; ++i)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) v[i][q] = kb + i < k1 ? src_of(kb + i)[(size_t)q * H] : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int i = 0; i < kKB; ++i) {
           const int k = kb + i;
-          const float lk = k < k1 ? lse_of(k) : -INFINITY;
+          const float lk = k >= k1 ? -INFINITY : (kb == k0 ? l8[i] : lse_of(k));
           w[i] = lk == -INFINITY ? 0.f : expf(lk - m);
-          const uint4* src = reinterpret_cast<const uint4*>(plan.o_part) +
-                             (((size_t)min(k, k1 - 1) * n_q + j) * (kDC / 8) + c0 / 8) * H + h;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) v[i][q] = k < k1 ? src[(size_t)q * H] : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < kKB; ++i) {

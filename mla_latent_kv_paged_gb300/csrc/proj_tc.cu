@@ -80,15 +80,6 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // rotated positional query: copied unchanged next to the absorbed one
-  if (kAbsorb && cblk == 0) {
-    for (int i = threadIdx.x; i < T * (kDR / 8); i += kThreads) {
-      const int t = i / (kDR / 8), v = i % (kDR / 8);
-      const uint4 w = reinterpret_cast<const uint4*>(q_rope + ((size_t)t * H + h) * kDR)[v];
-      reinterpret_cast<uint4*>(out + ((size_t)t * H + h) * kRow + kDC)[v] = w;
-    }
-  }
-
   const uint32_t idesc = idesc_bf16(128, C::NT, kAbsorb, false);
   auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };
   const uint64_t bdesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffB);
@@ -133,6 +124,15 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         }
       }
       mma_commit(bar_d);  // arrives once the MMAs (if any) finished
+    }
+    // rotated positional query, copied unchanged next to the absorbed one, by
+    // warps 1..3 while thread 0 waits for the tiles
+    if (kAbsorb && cblk == 0 && t0 == 0 && warp > 0) {
+      for (int i = threadIdx.x - 32; i < T * (kDR / 8); i += kThreads - 32) {
+        const int t = i / (kDR / 8), v = i % (kDR / 8);
+        const uint4 w = reinterpret_cast<const uint4*>(q_rope + ((size_t)t * H + h) * kDR)[v];
+        reinterpret_cast<uint4*>(out + ((size_t)t * H + h) * kRow + kDC)[v] = w;
+      }
     }
     __syncwarp();
     if (!wait_phase(bar_d, phase, abort_flag, err_word)) break;
