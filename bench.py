@@ -4,8 +4,13 @@ Default workload: DeepSeek-V3-shaped decode, B=32 sequences x context 4096,
 H=128 heads, page 64, one query token per sequence (seeded synthetic data,
 random weights). One step = mla_absorb_q -> mla_decode_paged -> mla_combine
 -> mla_out_proj for the whole batch; tokens/s = query tokens per step / step
-time. L2 is flushed (a 256 MiB write) between timed steps; each step is timed
-with CUDA events on the launching stream.
+time. Steps run back to back (CUDA graphs of consecutive steps) over three
+complete input sets at distinct addresses used in rotation, so every step reads
+inputs that are no longer in L2 (the sets together are ~4.5x the L2); the timed
+region is bracketed by CUDA events on the launching stream. The JSON line also
+carries per-call phase times (each call back to back over the same rotation),
+the decode call's roofline, one step replayed alone after an L2 flush, and the
+end-to-end rate through the Python API with host copies.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -36,6 +41,8 @@ import mla_inputs as mi  # noqa: E402
 METRIC = "MLA decode tokens/s & latent-KV HBM GB/s (% of GB300 roofline), 1 GPU"
 UNIT = "tokens/s"
 WORKLOAD_INDEX = 2
+NSETS = 3        # rotating input sets in the timed region
+ROTATIONS = 10   # passes over the sets per graph replay
 
 
 def peaks():
@@ -170,7 +177,8 @@ def workload_config(inp, num_splits):
                         f"{int(inp.seq_lens[0])}, H={inp.H}, d_c=512, d_r=64, page 64, n_q={inp.n_q}",
             "batch": inp.B, "context": int(inp.seq_lens[0]), "heads": inp.H, "n_q": inp.n_q,
             "page_size": 64, "num_splits": num_splits, "cache_bytes": int(inp.seq_lens.sum()) * 1152,
-            "l2": "flushed between timed steps (256 MiB write)"}
+            "l2": f"inputs larger than L2: {NSETS} rotating input sets of ~190 MB (latent cache, weights, "
+                  "queries, tables), steps back to back, no flush"}
 
 
 def run_ours(args):
@@ -193,60 +201,70 @@ def run_ours(args):
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    q_nope = to_dev(inp.q_nope.reshape(T, H, -1))
-    q_rope = to_dev(inp.q_rope.reshape(T, H, -1))
-    w_uk, w_uv = to_dev(inp.w_uk), to_dev(inp.w_uv)
-    cache = to_dev(pg.cache)
-    bt = torch.from_numpy(pg.block_table).to(dev)
-    sl = torch.from_numpy(inp.seq_lens).to(dev)
     G = mla.default_splits(n_q)
-    bufs = dict(q_abs=torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev),
-                workspace=torch.empty(mla.workspace_bytes(B, n_q, H, G), dtype=torch.uint8, device=dev),
-                u=torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
-                lse=torch.empty((T, H), dtype=torch.float32, device=dev),
-                out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev))
+    # NSETS complete input sets (queries, weights, latent cache, block table,
+    # lengths, work buffers) at distinct addresses, used in rotation: a step
+    # touches ~190 MB, so the set a step reads was last touched NSETS - 1 steps
+    # (~380 MB of other traffic) earlier and is no longer in the 126 MB L2.
+    # Consecutive steps run back to back, as consecutive layers of a serving
+    # loop would; no L2 flush is needed between them.
+    sets = []
+    for _ in range(NSETS):
+        sets.append(dict(
+            q_nope=to_dev(inp.q_nope.reshape(T, H, -1)), q_rope=to_dev(inp.q_rope.reshape(T, H, -1)),
+            w_uk=to_dev(inp.w_uk), w_uv=to_dev(inp.w_uv), cache=to_dev(pg.cache),
+            bt=torch.from_numpy(pg.block_table).to(dev), sl=torch.from_numpy(inp.seq_lens).to(dev),
+            q_abs=torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev),
+            workspace=torch.empty(mla.workspace_bytes(B, n_q, H, G), dtype=torch.uint8, device=dev),
+            u=torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+            lse=torch.empty((T, H), dtype=torch.float32, device=dev),
+            out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)))
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        q_abs = mla.absorb_q(q_nope, q_rope, w_uk, bufs["q_abs"])
-        mla.decode_paged(q_abs, cache, bt, sl, n_q=n_q, num_splits=G, workspace=bufs["workspace"],
-                         err_word=err)
-        mla.combine(bufs["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=bufs["u"], lse=bufs["lse"])
-        mla.out_proj(bufs["u"], w_uv, bufs["out"])
+    def absorb(S):
+        mla.absorb_q(S["q_nope"], S["q_rope"], S["w_uk"], S["q_abs"])
 
-    # eager warm-up (compiles nothing; checks the error word), then one CUDA graph
-    # holding the whole step so the timed region measures device time only
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    def decode(S):
+        mla.decode_paged(S["q_abs"], S["cache"], S["bt"], S["sl"], n_q=n_q, num_splits=G,
+                         workspace=S["workspace"], err_word=err)
+
+    def combine(S):
+        mla.combine(S["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=S["u"], lse=S["lse"])
+
+    def out_proj(S):
+        mla.out_proj(S["u"], S["w_uv"], S["out"])
+
+    def step(S):
+        absorb(S)
+        decode(S)
+        combine(S)
+        out_proj(S)
+
+    # eager warm-up (checks the error word), then CUDA graphs of back-to-back
+    # steps so the timed region measures device time, not host launches
+    for k in range(args.warmup):
+        step(sets[k % NSETS])
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
+
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             fn()
         return g
 
-    graph = capture(step)
-    # one graph per call, for the per-kernel phase times
-    sub = [
-        capture(lambda: mla.absorb_q(q_nope, q_rope, w_uk, bufs["q_abs"])),
-        capture(lambda: mla.decode_paged(bufs["q_abs"], cache, bt, sl, n_q=n_q, num_splits=G,
-                                         workspace=bufs["workspace"], err_word=err)),
-        capture(lambda: mla.combine(bufs["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=bufs["u"],
-                                    lse=bufs["lse"])),
-        capture(lambda: mla.out_proj(bufs["u"], w_uv, bufs["out"])),
-    ]
-    for _ in range(args.warmup):
-        flush.zero_()
+    R = min(args.steps, ROTATIONS * NSETS)  # steps per graph replay
+    graph = capture(lambda: [step(sets[k % NSETS]) for k in range(R)])
+    rest = args.steps % R
+    graph_rest = capture(lambda: [step(sets[k % NSETS]) for k in range(rest)]) if rest else None
+    for _ in range(max(1, args.warmup // R)):
         graph.replay()
     torch.cuda.synchronize()
 
-    t_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0_ev, t1_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -254,38 +272,56 @@ def run_ours(args):
     clocks.start()
     time.sleep(0.3)
     wall0 = time.perf_counter()
-    for k in range(args.steps):
-        flush.zero_()
-        t_start[k].record(stream)
+    t0_ev.record(stream)
+    for _ in range(args.steps // R):
         graph.replay()
-        t_end[k].record(stream)
+    if graph_rest is not None:
+        graph_rest.replay()
+    t1_ev.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    step_ms = np.array([t_start[k].elapsed_time(t_end[k]) for k in range(args.steps)])
-    total_ms = float(step_ms.sum())
+    total_ms = t0_ev.elapsed_time(t1_ev)
     if dist is not None:
         t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     value = ws_ * T * args.steps / (total_ms * 1e-3)
-    # per-kernel phase times: the four calls replayed as separate graphs behind a
-    # short device-side sleep, so every launch is queued before the first event
-    n_phase = min(args.steps, 200)
-    pev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    phase = np.zeros((n_phase, 4))
-    for k in range(n_phase):
-        flush.zero_()
-        torch.cuda._sleep(200000)
-        pev[0].record(stream)
-        for i in range(4):
-            sub[i].replay()
-            pev[i + 1].record(stream)
+
+    # per-call phase times: each call alone, R times back to back over the
+    # rotating sets in one graph (the decode call is the plan and decode kernels)
+    def per_call_us(fn, reps=20):
+        g = capture(lambda: [fn(sets[k % NSETS]) for k in range(R)])
+        g.replay()
         torch.cuda.synchronize()
-        phase[k] = [pev[i].elapsed_time(pev[i + 1]) for i in range(4)]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in ev:
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])) / R
+
+    phases = {"absorb_q": per_call_us(absorb), "decode_paged": per_call_us(decode),
+              "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
+    # for reference: one step replayed alone after an L2 flush (cold caches,
+    # including the graph launch, about 6.6 us on this system)
+    g1 = capture(lambda: step(sets[0]))
+    single = []
+    for _ in range(50):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g1.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        single.append(1e3 * e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error word {int(err.item())}")
 
     # ---------------------------------------------------------------- end to end
     # Per step: the new queries, block table and context lengths go host->device
@@ -302,7 +338,9 @@ def run_ours(args):
     h2d = h_qn.numel() * 2 + h_qr.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
-    captured = mla.CapturedStep(w_uk, w_uv, cache, bt, sl, n_q=n_q, num_splits=G, err_word=err)
+    S0 = sets[0]
+    bt, sl = S0["bt"], S0["sl"]
+    captured = mla.CapturedStep(S0["w_uk"], S0["w_uv"], S0["cache"], bt, sl, n_q=n_q, num_splits=G, err_word=err)
 
     def e2e_step():
         bt.copy_(h_bt, non_blocking=True)
@@ -331,28 +369,28 @@ def run_ours(args):
     if rank == 0:
         hbm, tflops, src = peaks()
         wb = mi.workload_bytes(inp)
-        dec_ms = float(phase[:, 1].mean())
+        dec_us = phases["decode_paged"]
         dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
-        achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+        achieved = dec_bytes / (dec_us * 1e-6) / 1e9
         traffic = stored_traffic()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(inp, G),
-            "phases_us": {"absorb_q": 1e3 * float(phase[:, 0].mean()),
-                          "decode_paged": 1e3 * dec_ms,
-                          "combine": 1e3 * float(phase[:, 2].mean()),
-                          "out_proj": 1e3 * float(phase[:, 3].mean())},
+            "phases_us": phases,
+            "single_step_flushed_us": float(np.median(single)),
             "roofline": {"kernel": "mla_decode_paged (plan + split-KV decode kernels)", "bound": "hbm",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": src,
                          "alg_bytes_per_launch": dec_bytes, "alg_flops_per_launch": wb["decode_flops"],
-                         "tflops_achieved": wb["decode_flops"] / (dec_ms * 1e-3) / 1e12,
-                         "tensor_peak_tflops": tflops},
+                         "tflops_achieved": wb["decode_flops"] / (dec_us * 1e-6) / 1e12,
+                         "tensor_peak_tflops": tflops,
+                         "duration": f"per call, {R} calls back to back over {NSETS} rotating input sets"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 5 * args.steps,
-            "timing": "CUDA-graph replay of the whole step; events on the launching stream",
+            "timing": (f"CUDA events around the timed region: graphs of {R} back-to-back steps over "
+                       f"{NSETS} rotating input sets, replayed until {args.steps} steps ran"),
             "clocks": clk,
             "wall_s_timed_region": wall,
         }
