@@ -305,6 +305,14 @@ def run_ours(args):
         torch.cuda.synchronize()
         return 1e3 * float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])) / R
 
+    if args.quick:  # timed region only (short profiling runs)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                              "quick": True, "config": workload_config(inp, G)}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     phases = {"absorb_q": per_call_us(absorb), "decode_paged": per_call_us(decode),
               "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
     # for reference: one step replayed alone after an L2 flush (cold caches,
@@ -432,6 +440,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="time the steps only (no phase times, end-to-end leg or CPU baseline): for profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
