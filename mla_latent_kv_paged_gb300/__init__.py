@@ -270,10 +270,19 @@ class CapturedStep:
     queries in (from host or device tensors, asynchronously) and replays the
     graph on the current stream; the returned tensors are the step's own
     buffers, overwritten by the next call.
+
+    With ``host_io=True`` the step also owns pinned host buffers (``.host``:
+    q_nope, q_rope, block_table, seq_lens in; out, lse out), packed into one
+    input and one output area, and a second graph that copies the inputs to
+    the device in one copy, runs the step on them and copies out and lse back
+    in one copy. One serving step is then: write the new inputs into
+    ``.host``, call ``replay_host()``, synchronise the stream, read
+    ``.host["out"]``. (That graph uses the block table and lengths of
+    ``.host``, not the block_table / seq_lens tensors given here.)
     """
 
     def __init__(self, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
-                 softmax_scale: float = DEFAULT_SCALE, err_word=None):
+                 softmax_scale: float = DEFAULT_SCALE, err_word=None, host_io: bool = False):
         import torch
         B = block_table.shape[0]
         H = w_uk.shape[0]
@@ -301,6 +310,45 @@ class CapturedStep:
         with torch.cuda.graph(self.graph):
             decode_step(*args, **kw)
         self.num_splits = g
+        self.host = None
+        if host_io:
+            # one packed input and one packed output area, on the device and pinned
+            # on the host, so a replay moves each direction in a single copy
+            def layout(parts):
+                off, views = 0, {}
+                for name, shape, dtype in parts:
+                    n = math.prod(shape) * torch.tensor([], dtype=dtype).element_size()
+                    views[name] = (off, n, shape, dtype)
+                    off = (off + n + 255) // 256 * 256
+                return off, views
+
+            def carve(buf, views):
+                return {k: buf[o:o + n].view(dt).view(shape) for k, (o, n, shape, dt) in views.items()}
+
+            in_bytes, in_views = layout([("q_nope", self.q_nope.shape, bf), ("q_rope", self.q_rope.shape, bf),
+                                         ("block_table", block_table.shape, torch.int32),
+                                         ("seq_lens", seq_lens.shape, torch.int32)])
+            out_bytes, out_views = layout([("out", (T, H, D_V), bf), ("lse", (T, H), torch.float32)])
+            self._dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
+            self._dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
+            self._host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+            self._host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
+            d_in, d_out = carve(self._dev_in, in_views), carve(self._dev_out, out_views)
+            self.host = {**carve(self._host_in, in_views), **carve(self._host_out, out_views)}
+            self.host["block_table"].copy_(block_table.cpu())
+            self.host["seq_lens"].copy_(seq_lens.cpu())
+            io_bufs = dict(self.bufs, out=d_out["out"], lse=d_out["lse"])
+            io_args = (d_in["q_nope"], d_in["q_rope"], w_uk, w_uv, cache, d_in["block_table"], d_in["seq_lens"])
+            io_kw = dict(kw, bufs=io_bufs)
+
+            def io_step():
+                self._dev_in.copy_(self._host_in, non_blocking=True)
+                decode_step(*io_args, **io_kw)
+                self._host_out.copy_(self._dev_out, non_blocking=True)
+
+            self.graph_io = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph_io):
+                io_step()
 
     def __call__(self, q_nope=None, q_rope=None):
         """q_nope [T,H,128], q_rope [T,H,64] (bf16, host or device); None keeps the previous ones."""
@@ -310,3 +358,11 @@ class CapturedStep:
             self.q_rope.copy_(q_rope, non_blocking=True)
         self.graph.replay()
         return dict(q_abs=self.bufs["q_abs"], u=self.bufs["u"], lse=self.bufs["lse"], out=self.bufs["out"])
+
+    def replay_host(self):
+        """One step from and to the pinned host buffers ``.host`` (``host_io=True``):
+        inputs copied in, the step, out and lse copied back, all inside one graph
+        replay on the current stream. Synchronise before reading ``.host``."""
+        if self.host is None:
+            raise RuntimeError("CapturedStep was built without host_io=True")
+        self.graph_io.replay()

@@ -105,6 +105,42 @@ def test_captured_step_replays_equal_eager_steps(mla):
     compare_full(inp2, r2)
 
 
+def test_captured_step_host_io_copies_inside_the_graph(mla):
+    """host_io=True: inputs from pinned host buffers, results back to them, in one replay;
+    the same bits as the eager step, and new host inputs are picked up by the next replay."""
+    import torch
+    inp = mi.make_inputs(B=3, H=128, n_q=1, seq_lens=[70, 300, 129], seed=79)
+    pg = mi.make_paged(inp, spare_pages=8)
+    d = device_inputs(inp, pg)
+    step = mla.CapturedStep(d["w_uk"], d["w_uv"], d["cache"], d["block_table"], d["seq_lens"], n_q=1,
+                            num_splits=5, host_io=True)
+    h = step.host
+    h["q_nope"].copy_(d["q_nope"].cpu())
+    h["q_rope"].copy_(d["q_rope"].cpu())
+    step.replay_host()
+    torch.cuda.synchronize()
+    e = mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], d["block_table"],
+                        d["seq_lens"], n_q=1, num_splits=5)
+    torch.cuda.synchronize()
+    assert torch.equal(h["out"].view(torch.int16), e["out"].cpu().view(torch.int16))
+    assert torch.equal(h["lse"], e["lse"].cpu())
+    # a shorter context for sequence 1 (its first 200 rows), written into the host buffer only
+    import dataclasses
+    L = inp.seq_lens.copy()
+    L[1] = 200
+    off = inp.seq_off
+    keep = np.concatenate([np.arange(off[0], off[1]), np.arange(off[1], off[1] + 200), np.arange(off[2], off[3])])
+    inp2 = dataclasses.replace(inp, seq_lens=L.astype(np.int32),
+                               seq_off=np.concatenate([[0], np.cumsum(L)]).astype(np.int64),
+                               c=inp.c[keep], kr=inp.kr[keep])
+    h["seq_lens"].copy_(torch.from_numpy(inp2.seq_lens))
+    step.replay_host()
+    torch.cuda.synchronize()
+    ref = oracle.absorbed_f64(inp2)
+    assert_close(dev_bf16_to_f64(h["out"]).reshape(-1, 128), ref["out"], "out")
+    assert_close(h["lse"].double().numpy().reshape(-1), ref["lse"], "lse")
+
+
 def test_combine_alone_merges_oracle_partials(mla):
     """Feed oracle partials through the documented workspace layout into mla_combine."""
     import torch
