@@ -38,6 +38,8 @@ PINS = {
     "absorbed_f32": "baseline only (timed); agrees with the fp64 path to fp32 rounding",
     "absorb_q_f64": "pinned: numpy matmul; equals the q_abs of absorbed_f64",
     "out_proj_f64": "pinned: numpy matmul; W_UV applied to absorbed_f64's u gives its out",
+    "append_f64": "pinned: numpy matmul; the generator's rotation; identity weights; position 0; "
+                  "norm and relative-position properties of the rotation",
 }
 
 
@@ -264,3 +266,22 @@ def out_proj_f64(u_bits, w_uv_bits):
     lib.mla_oracle_out_proj_f64(_p(u), _p(wv), ctypes.c_int64(T), ctypes.c_int(H), ctypes.c_int(d_c),
                                 ctypes.c_int(d_v), _p(out))
     return out
+
+
+def append_f64(h_bits: np.ndarray, w_dkr_bits: np.ndarray, pos, theta: float = 10000.0, d_c: int = 512):
+    """Cache rows of new tokens: [c (d_c) ; rotated k^R (d_r)] for h [T][d_model] and the
+    transposed weights w_dkr [d_c + d_r][d_model] (bf16 bits), positions pos [T]."""
+    L = _load()
+    h = np.ascontiguousarray(h_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_dkr_bits, dtype=np.uint16)
+    T, d_model = h.shape
+    D = w.shape[0]
+    assert w.shape[1] == d_model and D > d_c and (D - d_c) % 2 == 0
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    assert p.shape == (T,)
+    out = np.zeros((T, D), dtype=np.float64)
+    L.mla_oracle_append_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_void_p]
+    L.mla_oracle_append_f64(_p(h), _p(w), _p(p), T, d_model, d_c, D - d_c, float(theta), _p(out))
+    return out
+

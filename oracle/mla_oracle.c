@@ -485,3 +485,38 @@ int mla_oracle_out_proj_f64(const uint16_t* u, const uint16_t* w_uv, int64_t T, 
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------- cache append */
+/* Latent-cache row of a new token (Huny section 1.2: c_t^KV = h_t W^DKV, the
+ * joint low-rank compression; section 2.2: the decoupled positional key
+ * k^R_t = RoPE(h_t W^KR), shared by all heads and cached already rotated).
+ * The weights come transposed, one row per output column: w_dkr[i][k] for
+ * i < d_c is W^DKV[k][i], for d_c <= i < d_c + d_r it is W^KR[k][i - d_c].
+ * For new row t at position pos[t]:
+ *   row[t][i]       = sum_k h[t][k] w_dkr[i][k]                 (i < d_c)
+ *   k[e]            = sum_k h[t][k] w_dkr[d_c + e][k]           (e < d_r)
+ *   (row[t][d_c+2i], row[t][d_c+2i+1]) = (k[2i] cos a - k[2i+1] sin a,
+ *                                         k[2i] sin a + k[2i+1] cos a),
+ *   a = pos[t] * theta^(-2i / d_r)
+ * (the rotation R_t of the pages, applied to consecutive pairs). */
+int mla_oracle_append_f64(const uint16_t* h, const uint16_t* w_dkr, const int64_t* pos, int64_t T, int d_model,
+                          int d_c, int d_r, double theta, double* row_out) {
+    const int D = d_c + d_r;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double* row = row_out + t * D;
+        for (int i = 0; i < D; ++i) {
+            double acc = 0.0;
+            for (int k = 0; k < d_model; ++k) acc += bf(h[t * d_model + k]) * bf(w_dkr[(int64_t)i * d_model + k]);
+            row[i] = acc;
+        }
+        for (int i = 0; i < d_r / 2; ++i) {
+            const double a = (double)pos[t] * pow(theta, -2.0 * i / d_r);
+            const double x = row[d_c + 2 * i], y = row[d_c + 2 * i + 1];
+            row[d_c + 2 * i] = x * cos(a) - y * sin(a);
+            row[d_c + 2 * i + 1] = x * sin(a) + y * cos(a);
+        }
+    }
+    return 0;
+}
+

@@ -235,3 +235,52 @@ def test_single_step_functions(tiny):
     # W_UV applied to the absorbed path's own u reproduces its out
     o_full = np.einsum("hvc,thc->thv", f64(tiny.w_uv), full["u"].reshape(T, tiny.H, 512))
     assert np.abs(o_full.reshape(-1, 128) - full["out"]).max() <= 1e-11
+
+
+# ------------------------------------------------------------------ cache append
+def _append_case(T=5, d_model=96, seed=3):
+    rng = np.random.default_rng(seed)
+    h = mi.f32_to_bf16(rng.standard_normal((T, d_model)).astype(np.float32))
+    w = mi.f32_to_bf16((rng.standard_normal((576, d_model)) / math.sqrt(d_model)).astype(np.float32))
+    pos = np.array([0, 1, 63, 64, 131071][:T], dtype=np.int64)
+    return h, w, pos
+
+
+def test_append_latent_part_is_the_plain_projection():
+    """Huny section 1.2: c_t = h_t W^DKV, checked against numpy's matmul."""
+    h, w, pos = _append_case()
+    r = oracle.append_f64(h, w, pos)
+    assert np.abs(r[:, :512] - f64(h) @ f64(w[:512]).T).max() < 1e-12
+
+
+def test_append_positional_part_matches_the_generator_rotation():
+    """Section 2.2: k^R_t = RoPE(h_t W^KR), against the input generator's own rotation code."""
+    h, w, pos = _append_case()
+    r = oracle.append_f64(h, w, pos)
+    k = f64(h) @ f64(w[512:]).T
+    assert np.abs(r[:, 512:] - mi.rope_rotate(k, pos)).max() < 1e-10
+    # position 0 is the identity rotation
+    assert np.array_equal(r[0, 512:], k[0])
+
+
+def test_append_identity_weights_and_rotation_properties():
+    """W = I (d_model = 576): the row is h with its last 64 values rotated; the rotation keeps
+    every pair's norm, and the dot of two rotated vectors depends only on the position gap."""
+    rng = np.random.default_rng(5)
+    T = 4
+    h = mi.f32_to_bf16(rng.standard_normal((T, 576)).astype(np.float32))
+    eye = mi.f32_to_bf16(np.eye(576, dtype=np.float32))
+    pos = np.array([3, 10, 1000, 1007], dtype=np.int64)
+    r = oracle.append_f64(h, eye, pos)
+    assert np.array_equal(r[:, :512], f64(h)[:, :512])
+    x = f64(h)[:, 512:]
+    pairs_in = x[:, 0::2] ** 2 + x[:, 1::2] ** 2
+    pairs_out = r[:, 512::2] ** 2 + r[:, 513::2] ** 2
+    assert np.abs(pairs_in - pairs_out).max() < 1e-12 * max(1.0, pairs_in.max())
+    # same inputs at positions (3, 10) and (1000, 1007): the same gap of 7, the same dot
+    same = np.vstack([x[0], x[1], x[0], x[1]])
+    h2 = np.hstack([f64(h)[:, :512], same])
+    r2 = oracle.append_f64(mi.f32_to_bf16(h2.astype(np.float32)), eye, pos)
+    d1 = r2[0, 512:] @ r2[1, 512:]
+    d2 = r2[2, 512:] @ r2[3, 512:]
+    assert abs(d1 - d2) < 1e-9 * max(1.0, abs(d1))
