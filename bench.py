@@ -42,6 +42,7 @@ METRIC = "MLA decode tokens/s & latent-KV HBM GB/s (% of GB300 roofline), 1 GPU"
 UNIT = "tokens/s"
 WORKLOAD_INDEX = 2
 NSETS = 3        # rotating input sets in the timed region
+D_MODEL = 7168   # hidden width of the cache-append phase (DeepSeek-V3)
 ROTATIONS = 10   # passes over the sets per graph replay
 
 
@@ -208,9 +209,14 @@ def run_ours(args):
     # (~380 MB of other traffic) earlier and is no longer in the 126 MB L2.
     # Consecutive steps run back to back, as consecutive layers of a serving
     # loop would; no L2 flush is needed between them.
+    rng = np.random.default_rng(7168)
+    h_bits = mi.f32_to_bf16(rng.standard_normal((T, D_MODEL)).astype(np.float32))
+    w_dkr_bits = mi.f32_to_bf16((rng.standard_normal((576, D_MODEL)) / np.sqrt(D_MODEL)).astype(np.float32))
     sets = []
     for _ in range(NSETS):
         sets.append(dict(
+            h=to_dev(h_bits), w_dkr=to_dev(w_dkr_bits),
+            ws_app=torch.zeros(mla.append_workspace_bytes(T, D_MODEL), dtype=torch.uint8, device=dev),
             q_nope=to_dev(inp.q_nope.reshape(T, H, -1)), q_rope=to_dev(inp.q_rope.reshape(T, H, -1)),
             w_uk=to_dev(inp.w_uk), w_uv=to_dev(inp.w_uv), cache=to_dev(pg.cache),
             bt=torch.from_numpy(pg.block_table).to(dev), sl=torch.from_numpy(inp.seq_lens).to(dev),
@@ -235,6 +241,10 @@ def run_ours(args):
 
     def out_proj(S):
         mla.out_proj(S["u"], S["w_uv"], S["out"])
+
+    def append(S):  # the cache-append step (not part of the timed decode step)
+        mla.append_kv(S["h"], S["w_dkr"], S["cache"], S["bt"], S["sl"], n_q=n_q, workspace=S["ws_app"],
+                      err_word=err)
 
     def step(S):
         absorb(S)
@@ -315,6 +325,7 @@ def run_ours(args):
         return
     phases = {"absorb_q": per_call_us(absorb), "decode_paged": per_call_us(decode),
               "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
+    append_us = per_call_us(append)
     # for reference: one step replayed alone after an L2 flush (cold caches,
     # including the graph launch, about 6.6 us on this system)
     g1 = capture(lambda: step(sets[0]))
@@ -391,6 +402,7 @@ def run_ours(args):
                          "tensor_peak_tflops": tflops,
                          "duration": f"per call, {R} calls back to back over {NSETS} rotating input sets"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "append_kv": append_line(append_us, T, hbm),
             "gpu_launches": 5 * args.steps,
             "timing": (f"CUDA events around the timed region: graphs of {R} back-to-back steps over "
                        f"{NSETS} rotating input sets, replayed until {args.steps} steps ran"),
@@ -402,6 +414,15 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def append_line(us, T, hbm):
+    """The cache-append call (c = h W^DKV, k^R = RoPE(h W^KR) into the pages): its time per call
+    and its HBM roofline (weights + hidden states read, the new rows written)."""
+    alg = 576 * D_MODEL * 2 + T * D_MODEL * 2 + T * 576 * 2
+    gbs = alg / (us * 1e-6) / 1e9
+    return {"us": us, "d_model": D_MODEL, "rows": T, "alg_bytes": alg, "achieved_gbs": gbs, "peak_gbs": hbm,
+            "frac": gbs / hbm, "bound": "hbm"}
 
 
 def stored_traffic():

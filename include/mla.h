@@ -193,6 +193,39 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache,
 mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
                         int T, int H, int d_c, int d_v, void* stream);
 
+/* ------------------------------------------------------------------------
+ * mla_append_kv — the latent-cache rows of the new tokens, written into their
+ * pages (the step before decoding them):
+ *   row[i] = sum_k h[t][k] w_dkr[i][k]         i < 576
+ *   (row[512 + 2i], row[513 + 2i]) rotated by the angle pos * rope_theta^(-2i/64)
+ *   cache[block_table[b][pos / 64]][pos % 64][0:576] = row (bf16, nearest even)
+ * for new row t = b * n_q + j at position pos = L - n_q + j, L = seq_lens[b]
+ * (which already counts the new tokens). Huny's Dev Blog section 1.2: the
+ * joint compression c_t^KV = h_t W^DKV; section 2.2: the decoupled positional
+ * key k^R_t = RoPE(h_t W^KR), shared by the heads and cached already rotated
+ * (consecutive pairs, the convention of the input rows mla_decode_paged reads).
+ *   h           [B][n_q][d_model] bf16 hidden states of the new tokens
+ *   w_dkr       [576][d_model] bf16: rows 0..511 hold W^DKV transposed
+ *               (w_dkr[i][k] = W^DKV[k][i]), rows 512..575 W^KR transposed
+ *   cache, block_table, seq_lens, page_size, max_pages_per_seq: as for
+ *               mla_decode_paged; only the new rows are written
+ *   d_model     a multiple of 64, at most 65536
+ *   workspace   >= mla_append_workspace_bytes(B * n_q, d_model) bytes: fp32
+ *               partial sums of the d_model reduction (split across CTAs);
+ *               no initial contents needed. Calls sharing a workspace must
+ *               not overlap on the GPU.
+ * The sums over d_model are added in a fixed order, so results are
+ * reproducible bit for bit. A context length outside [n_q, max_pages * 64]
+ * is clamped and a page id outside [0, num_pages) skips that row; both are
+ * reported in err_word as MLA_ERR_BOUNDS. Starts after the kernel before it
+ * on the stream has finished (h is usually that kernel's output). */
+size_t mla_append_workspace_bytes(int T, int d_model);
+mla_status mla_append_kv(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache,
+                         const int32_t* block_table, const int32_t* seq_lens, int B, int n_q,
+                         int d_model, int num_pages, int page_size, int max_pages_per_seq,
+                         float rope_theta, void* workspace, size_t workspace_bytes,
+                         int32_t* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

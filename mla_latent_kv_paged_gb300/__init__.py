@@ -43,6 +43,7 @@ EXPORTS = [
     "mla_absorb_q", "mla_decode_default_splits", "mla_decode_workspace_bytes",
     "mla_decode_paged", "mla_combine", "mla_out_proj",
     "mla_decode_noalloc_max_bytes", "mla_decode_noalloc",
+    "mla_append_workspace_bytes", "mla_append_kv",
 ]
 
 
@@ -92,6 +93,10 @@ def lib():
             L.mla_decode_noalloc_max_bytes.restype = sz
             L.mla_decode_noalloc.restype = i
             L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
+            L.mla_append_workspace_bytes.restype = sz
+            L.mla_append_workspace_bytes.argtypes = [i, i]
+            L.mla_append_kv.restype = i
+            L.mla_append_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp]
             _lib = L
     return _lib
 
@@ -222,6 +227,38 @@ def decode_noalloc(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits:
                                   num_splits, _ptr(_bits(u)), _ptr(lse), _ptr(err_word), _stream(stream))
     _check(st, "mla_decode_noalloc")
     return u, lse
+
+
+def append_workspace_bytes(T: int, d_model: int) -> int:
+    n = int(lib().mla_append_workspace_bytes(T, d_model))
+    if n == 0:
+        raise MlaError(1, "mla_append_workspace_bytes")
+    return n
+
+
+def append_kv(h, w_dkr, cache, block_table, seq_lens, *, n_q: int, rope_theta: float = 10000.0,
+              workspace=None, err_word=None, stream=None):
+    """Write the new tokens' cache rows: [h W^DKV ; RoPE(h W^KR)] into their pages.
+
+    h [B*n_q, d_model] (or [B, n_q, d_model]) bf16, w_dkr [576, d_model] bf16
+    (W^DKV and W^KR transposed, stacked), cache / block_table / seq_lens as for
+    decode_paged (seq_lens already counting the new tokens). The workspace (fp32
+    partial sums of the split d_model reduction; allocated when none is given)
+    is returned for reuse.
+    """
+    import torch
+    B, max_pages = block_table.shape
+    d_model = h.shape[-1]
+    need = append_workspace_bytes(B * n_q, d_model)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=h.device)
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    st = lib().mla_append_kv(_ptr(_bits(h)), _ptr(_bits(w_dkr)), _ptr(_bits(cache)), _ptr(block_table),
+                             _ptr(seq_lens), B, n_q, d_model, cache.shape[0], cache.shape[1], max_pages,
+                             float(rope_theta), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _ptr(err_word), _stream(stream))
+    _check(st, "mla_append_kv")
+    return workspace
 
 
 def out_proj(u, w_uv, out=None, stream=None):

@@ -133,4 +133,29 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, 
   return launch_status(launch_out_proj(u, w_uv, out, T, H, (cudaStream_t)stream));
 }
 
+size_t mla_append_workspace_bytes(int T, int d_model) {
+  if (T < 1 || T > 2 * MLA_MAX_BATCH || d_model < 64 || d_model % 64 != 0 || d_model > 65536) return 0;
+  return append_workspace_bytes(T, d_model);
+}
+
+mla_status mla_append_kv(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache, const int32_t* block_table,
+                         const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int page_size,
+                         int max_pages_per_seq, float rope_theta, void* workspace, size_t workspace_bytes,
+                         int32_t* err_word, void* stream) {
+  if (!h || !w_dkr || !cache || !block_table || !seq_lens || !workspace) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_dkr) || !aligned16(cache) || !aligned16(block_table) || !aligned16(seq_lens) ||
+      !aligned16(workspace))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || num_pages < 1 || max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.f) || rope_theta != rope_theta) return MLA_ERR_INVALID_ARG;
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || page_size != kPage) return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (d_model < 64 || d_model % 64 != 0 || d_model > 65536) return MLA_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
+    return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < append_workspace_bytes(B * n_q, d_model)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_append(h, w_dkr, cache, block_table, seq_lens, B, n_q, d_model, num_pages,
+                                     max_pages_per_seq, (double)rope_theta, workspace, err_word,
+                                     (cudaStream_t)stream));
+}
+
 }  // extern "C"

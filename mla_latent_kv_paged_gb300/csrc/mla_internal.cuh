@@ -130,5 +130,9 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, cons
                             uint16_t* q_abs, int T, int H, cudaStream_t s);
 cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
                             cudaStream_t s);
+size_t append_workspace_bytes(int T, int d_model);
+cudaError_t launch_append(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache, const int32_t* block_table,
+                          const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int max_pages,
+                          double theta, void* workspace, int32_t* err_word, cudaStream_t s);
 
 }  // namespace mla

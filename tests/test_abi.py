@@ -131,6 +131,32 @@ def test_host_validation_decode_and_combine(lib):
     assert lib.mla_combine(p, 2, 1, 16, 4, p + 4, p, None) == 1
 
 
+def test_host_validation_append(lib):
+    p = FAKE
+    ws = lib.mla_append_workspace_bytes(2, 512)
+    assert ws > 0
+    assert lib.mla_append_workspace_bytes(0, 512) == 0
+    assert lib.mla_append_workspace_bytes(2, 100) == 0
+    assert lib.mla_append_workspace_bytes(2, 0) == 0
+
+    def app(**kw):
+        a = dict(h=p, w=p, cache=p, bt=p, sl=p, B=2, n_q=1, d=512, num_pages=8, page=64, maxp=4, theta=1e4,
+                 ws=p, wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_append_kv(a["h"], a["w"], a["cache"], a["bt"], a["sl"], a["B"], a["n_q"], a["d"],
+                                 a["num_pages"], a["page"], a["maxp"], a["theta"], a["ws"], a["wsb"], a["err"], None)
+
+    assert app(h=None) == 1
+    assert app(cache=p + 2) == 1
+    assert app(B=0) == 1
+    assert app(theta=0.5) == 1
+    assert app(theta=float("nan")) == 1
+    assert app(n_q=3) == 2
+    assert app(d=96) == 2
+    assert app(page=128) == 2
+    assert app(wsb=ws - 1) == 3
+
+
 @pytest.mark.parametrize("lens,G", [([256, 256], 76), ([4096] * 32, 76), ([64] * 3, 2),
                                     ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5)])
 def test_plan_statement_covers_every_page_once(lens, G):
