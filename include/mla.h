@@ -26,6 +26,12 @@
  *     MLA_ERR_UNSUPPORTED_SHAPE without launching anything.
  *   - Argument errors found on the host return a status before any launch.
  *     A failed launch returns MLA_ERR_CUDA (cudaGetLastError is consumed).
+ *   - Kernels start while the kernel enqueued before them on the stream is
+ *     still finishing (programmatic dependent launch): mla_absorb_q and
+ *     mla_out_proj load their weights (w_uk, w_uv) in that time, so weights
+ *     must not be written by the kernel enqueued just before the call. Every
+ *     other input is read after that kernel has finished (and see
+ *     mla_decode_paged for its own rule).
  *   - Errors that only the device can see (a context length out of range, a
  *     page id outside [0, num_pages), a wait that timed out) are written as
  *     the first nonzero mla_status into *err_word (a device int32 the caller

@@ -64,9 +64,20 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     fence_mbar_init();
     prefetch_tmap(&map_a);
     prefetch_tmap(&map_b);
-    // this head's weights into L2 while the previous kernel finishes (one CTA
-    // per head for absorb_q, whose four column blocks share them)
-    if (!kAbsorb || cblk == 0) bulk_prefetch_l2(weights + (size_t)h * 128 * kDC, 128 * kDC * 2);
+    // this CTA's weight tiles into shared memory while the previous kernel
+    // finishes (weights are never that kernel's output); the activations
+    // follow after the grid dependency wait on the same barriers
+    const uint64_t pol = policy_evict_first();
+    if (kAbsorb) {
+      mbar_arrive_expect_tx(bar_ld, C::kABytes + C::kBBytes);
+      for (int m = 0; m < 2; ++m)  // W_UK[h][i][c] as boxes of [128 i][64 c]: this block's two halves
+        tma_load_3d(sbase + C::kOffA + m * C::kABox, &map_a, bar_ld, cblk * 128 + m * 64, 0, h, pol);
+    } else {
+      for (int kb = 0; kb < C::KB; ++kb) {
+        mbar_arrive_expect_tx(bar_ld + 8 * kb, C::kABox + C::kBBox);
+        tma_load_3d(sbase + C::kOffA + kb * C::kABox, &map_a, bar_ld + 8 * kb, kb * 64, 0, h, pol);
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmCols);
@@ -89,10 +100,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       const uint64_t pol = policy_evict_first();
       bool ok = true;
       if (kAbsorb) {
-        mbar_arrive_expect_tx(bar_ld, (t0 == 0 ? C::kABytes : 0) + C::kBBytes);
-        if (t0 == 0)  // W_UK[h][i][c] as boxes of [128 i][64 c]: the two 64-column halves of this block
-          for (int m = 0; m < 2; ++m)
-            tma_load_3d(sbase + C::kOffA + m * C::kABox, &map_a, bar_ld, cblk * 128 + m * 64, 0, h, pol);
+        if (t0 > 0) mbar_arrive_expect_tx(bar_ld, C::kBBytes);  // the first tile was armed with the weights
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(sbase + C::kOffB + kb * C::kBBox, &map_b, bar_ld, kb * 64, h, t0, pol);
         ok = wait_phase(bar_ld, phase, abort_flag, err_word);
@@ -108,8 +116,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       } else {
         for (int kb = 0; kb < C::KB; ++kb) {
           const uint32_t b = bar_ld + 8 * kb;
-          mbar_arrive_expect_tx(b, (t0 == 0 ? C::kABox : 0) + C::kBBox);
-          if (t0 == 0) tma_load_3d(sbase + C::kOffA + kb * C::kABox, &map_a, b, kb * 64, 0, h, pol);
+          if (t0 > 0) mbar_arrive_expect_tx(b, C::kBBox);  // the first tile was armed with the weights
           tma_load_3d(sbase + C::kOffB + kb * C::kBBox, &map_b, b, kb * 64, h, t0, pol);
         }
         const uint64_t adesc = smem_desc(0, 16, 1024, kSwizzle128B) + da(sbase + C::kOffA);
