@@ -91,9 +91,17 @@ mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const ui
 
 /* ------------------------------------------------------------------------
  * Split-KV decode. The pages of all sequences, taken in sequence order, are
- * cut into `num_splits` contiguous ranges of near-equal page count (range p
- * covers global pages [floor(p*P/num_splits), floor((p+1)*P/num_splits)),
- * P = total pages). One worker (a pair of CTAs on two SMs) processes one
+ * cut into G = min(num_splits, P) contiguous ranges of near-equal cost
+ * (P = total pages). A worker (a pair of CTAs on two SMs) that moves on to
+ * another sequence inside its range pays for the switch, so the pages are
+ * laid on a cost line where sequence b (n_b pages, first global page P_b)
+ * occupies [P_b + a*b, P_b + a*b + n_b) behind a switch stretch of a = 3
+ * points (for b >= 1); V = P + a*(B-1), and a = 0 instead when
+ * floor((P + 3*(B-1)) / G) < 4. Cut p (0 < p < G) sits at x = floor(p*V/G)
+ * and lands on global page P_b + max(0, x - P_b - a*b) of the last sequence
+ * b whose stretch starts at or before x (a cut inside a switch lands on the
+ * sequence start). Range p covers the pages from cut p to cut p+1 (cut 0 =
+ * page 0, cut G = P); ranges p >= G are empty. One worker processes one
  * range for one query index j. Where a range crosses a sequence boundary it
  * yields one partial per sequence it touches, so at most num_splits + B - 1
  * partials exist. The split points depend only on seq_lens and num_splits,

@@ -1,6 +1,10 @@
 // Split-KV work plan: cuts the pages of all sequences (in sequence order) into
-// G contiguous ranges of near-equal size and lists the (sequence, page range)
-// pieces each range covers. Flash-decoding over a paged cache: the Huny's Dev
+// G contiguous ranges of near-equal cost and lists the (sequence, page range)
+// pieces each range covers. A range that moves on to another sequence pays
+// for the switch (the accumulator of the finished piece is written out and
+// the next query is loaded), so every sequence start after the first counts
+// as kSwitchPages extra pages: the cuts are equal steps along that longer
+// line, and a cut that falls inside a switch lands on the sequence start. Flash-decoding over a paged cache: the Huny's Dev
 // Blog "MLA 아키텍처 해부" section 4 table names FlashDecoding / PagedAttention
 // as the decode techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
 //
@@ -13,6 +17,7 @@ namespace mla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kSwitchPages = 3;
 
 // Exclusive scan of v[0..n) in place (shared memory), returns the total.
 // Every thread of the block must call it.
@@ -86,13 +91,20 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   }
   __syncthreads();
   const int Ge = min(G, total);  // >= 1 since every sequence has >= 1 page
+  // Cost line: sequence b's pages sit at [Q_b, Q_b + n_b), Q_b = P_b + a*b,
+  // after a switch of a pages for b >= 1; length V = total + a*(B-1). Cut p
+  // sits at x_p = floor(p*V/Ge). The switch cost is dropped (a = 0) when a
+  // step along the line would not exceed it: steps of at least a+1 keep two
+  // cuts from landing on the same sequence start, so no range is empty.
+  const int64_t V0 = (int64_t)total + (int64_t)kSwitchPages * (B - 1);
+  const int64_t a = (V0 / Ge >= kSwitchPages + 1) ? kSwitchPages : 0;
+  const int64_t V = (int64_t)total + a * (B - 1);
 
-  // 2. pieces per sequence: interior boundaries x_p = floor(p*total/Ge),
-  //    p in [1, Ge-1], strictly inside (P_b, E_b)
+  // 2. pieces per sequence: cuts strictly inside (Q_b, Q_b + n_b)
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int64_t Pb = s_pstart[b], Eb = s_pstart[b + 1];
-    int64_t lo = ceil_div64((Pb + 1) * Ge, total);
-    int64_t hi = ceil_div64(Eb * Ge, total) - 1;
+    const int64_t Qb = s_pstart[b] + a * b, Eq = s_pstart[b + 1] + a * b;
+    int64_t lo = ceil_div64((Qb + 1) * Ge, V);
+    int64_t hi = ceil_div64(Eq * Ge, V) - 1;
     lo = max(lo, (int64_t)1);
     hi = min(hi, (int64_t)Ge - 1);
     s_istart[b] = 1 + (int)max((int64_t)0, hi - lo + 1);
@@ -111,12 +123,13 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   // 3. write the pieces of each sequence
   for (int b = tid; b < B; b += kPlanThreads) {
     const int64_t Pb = s_pstart[b], Eb = s_pstart[b + 1];
-    int64_t lo = max(ceil_div64((Pb + 1) * Ge, total), (int64_t)1);
-    int64_t hi = min(ceil_div64(Eb * Ge, total) - 1, (int64_t)Ge - 1);
+    const int64_t Qb = Pb + a * b, Eq = Eb + a * b;
+    int64_t lo = max(ceil_div64((Qb + 1) * Ge, V), (int64_t)1);
+    int64_t hi = min(ceil_div64(Eq * Ge, V) - 1, (int64_t)Ge - 1);
     int k = s_istart[b];
     int64_t start = Pb;
     for (int64_t p = lo; p <= hi; ++p) {
-      const int64_t x = (p * total) / Ge;
+      const int64_t x = (p * V) / Ge - a * b;  // global page of the cut
       plan.item_seq[k] = b;
       plan.item_page0[k] = (int)(start - Pb);
       plan.item_page1[k] = (int)(x - Pb);
@@ -138,19 +151,20 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     } else if (p >= Ge) {
       r = s_items;
     } else {
-      const int64_t x = ((int64_t)p * total) / Ge;
-      // largest b with P_b <= x (P strictly increasing)
+      const int64_t x = ((int64_t)p * V) / Ge;
+      // largest b whose stretch of the line (switch, then pages) starts at or
+      // before x: Q_b - a <= x for b >= 1 (strictly increasing in b)
       int lo = 0, hi = B - 1;
       while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
-        if (s_pstart[mid] <= x) lo = mid; else hi = mid - 1;
+        if (s_pstart[mid] + a * (mid - 1) <= x) lo = mid; else hi = mid - 1;
       }
       const int b = lo;
-      const int64_t Pb = s_pstart[b];
-      if (x == Pb) {
+      const int64_t Qb = s_pstart[b] + a * b;
+      if (x <= Qb) {  // on the switch into b or on its first page
         r = s_istart[b];
       } else {
-        const int64_t first = max(ceil_div64((Pb + 1) * Ge, total), (int64_t)1);
+        const int64_t first = max(ceil_div64((Qb + 1) * Ge, V), (int64_t)1);
         r = s_istart[b] + (int)(p - first + 1);
       }
     }

@@ -57,23 +57,36 @@ def device_inputs(inp, pg):
     )
 
 
-def plan_mirror(seq_lens, n_q, max_pages, G, page=64):
+def plan_mirror(seq_lens, n_q, max_pages, G, page=64, switch_pages=3):
     """Python statement of the split plan documented in include/mla.h (integer work):
-    pages of all sequences in order, cut at floor(p * P / G'), G' = min(G, P)."""
+    pages of all sequences in order, each sequence start after the first costing
+    `switch_pages` extra pages (dropped when a step is not longer than that);
+    cut p at floor(p * V / G') on that line, G' = min(G, P)."""
     lens = np.clip(np.asarray(seq_lens, dtype=np.int64), n_q, max_pages * page)
     pages = (lens + page - 1) // page
     starts = np.concatenate([[0], np.cumsum(pages)])
     P = int(starts[-1])
+    B = len(lens)
     Ge = min(G, P)
-    cuts = sorted(set([(p * P) // Ge for p in range(Ge + 1)]))
+    a = switch_pages if (P + switch_pages * (B - 1)) // Ge >= switch_pages + 1 else 0
+    V = P + a * (B - 1)
+
+    def to_page(x):  # a point of the cost line -> global page where the cut lands
+        line0 = [0] + [int(starts[b]) + a * (b - 1) for b in range(1, B)]
+        b = max(i for i in range(B) if line0[i] <= x)
+        return int(starts[b]) + max(0, x - (int(starts[b]) + a * b))
+
+    cut_at = [to_page((p * V) // Ge) for p in range(Ge + 1)]
+    assert all(x < y for x, y in zip(cut_at[:-1], cut_at[1:])), "an empty range"
+    cuts = sorted(set(cut_at))
     items = []  # (seq, page0, page1)
     seq_item = []
-    for b in range(len(lens)):
+    for b in range(B):
         seq_item.append(len(items))
         lo, hi = int(starts[b]), int(starts[b + 1])
         bounds = [lo] + [x for x in cuts if lo < x < hi] + [hi]
-        for a, z in zip(bounds[:-1], bounds[1:]):
-            items.append((b, a - lo, z - lo))
+        for x0, x1 in zip(bounds[:-1], bounds[1:]):
+            items.append((b, x0 - lo, x1 - lo))
     seq_item.append(len(items))
     range_item = []
     glob_start = [int(starts[b]) + p0 for (b, p0, _) in items]
@@ -81,7 +94,6 @@ def plan_mirror(seq_lens, n_q, max_pages, G, page=64):
         if p >= Ge:
             range_item.append(len(items))
         else:
-            x = (p * P) // Ge
-            range_item.append(glob_start.index(x))
+            range_item.append(glob_start.index(cut_at[p]))
     return dict(items=np.array(items, dtype=np.int64), seq_item=np.array(seq_item),
-                range_item=np.array(range_item), total=P, Ge=Ge, lens=lens)
+                range_item=np.array(range_item), total=P, Ge=Ge, lens=lens, switch=a)

@@ -158,10 +158,13 @@ def test_host_validation_append(lib):
 
 
 @pytest.mark.parametrize("lens,G", [([256, 256], 76), ([4096] * 32, 76), ([64] * 3, 2),
-                                    ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5)])
+                                    ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5),
+                                    ([4096] * 32, 38), ([64] * 500, 76), ([1] * 4096, 76),
+                                    ([640, 64, 64, 64, 640], 4), ([64 * 9] * 3, 6)])
 def test_plan_statement_covers_every_page_once(lens, G):
-    """The documented split plan: each range holds consecutive pages of near-equal
-    count; each sequence's pieces tile its pages in order."""
+    """The documented split plan: each range holds consecutive pages whose cost
+    (pages plus the switch cost for every further sequence it moves on to) is
+    near-equal; each sequence's pieces tile its pages in order."""
     pl = plan_mirror(lens, 1, 200, G)
     P, Ge = pl["total"], pl["Ge"]
     pages = (np.asarray(lens) + 63) // 64
@@ -171,11 +174,40 @@ def test_plan_statement_covers_every_page_once(lens, G):
         assert (its[:, 0] == b).all()
         assert its[0, 1] == 0 and its[-1, 2] == pages[b]
         assert (its[1:, 1] == its[:-1, 2]).all() and (its[:, 2] > its[:, 1]).all()
-    sizes = []
+    sizes, costs = [], []
+    a = pl["switch"]
     for p in range(G):
         its = pl["items"][pl["range_item"][p]:pl["range_item"][p + 1]]
+        assert (len(its) > 0) == (p < Ge)
         sizes.append(int((its[:, 2] - its[:, 1]).sum()) if len(its) else 0)
+        if len(its):
+            costs.append(sizes[-1] + a * (len(its) - 1))
     assert sum(sizes) == P
-    nz = [s for s in sizes if s]
-    assert max(nz) - min(nz) <= 1
+    # a step of the cost line is floor or ceil of V / G'; a range that starts on a
+    # sequence start may have been handed up to `a` points of the switch before it
+    assert max(costs) - min(costs) <= 1 + a
     assert len(pl["items"]) <= G + len(lens) - 1
+
+
+def test_plan_switch_cost_moves_pages_off_ranges_that_switch():
+    """32 sequences of 64 pages over 76 ranges: the ranges that hold a sequence
+    start inside them get about `switch` fewer pages than those that do not."""
+    pl = plan_mirror([4096] * 32, 1, 64, 76)
+    assert pl["switch"] == 3
+    one, two = [], []
+    for p in range(76):
+        its = pl["items"][pl["range_item"][p]:pl["range_item"][p + 1]]
+        n = int((its[:, 2] - its[:, 1]).sum())
+        (one if len(its) == 1 else two).append(n)
+    assert 24 <= len(two) <= 28 and max(two) <= 26 and min(one) >= 25
+    assert np.mean(one) - np.mean(two) >= 2
+    flat = plan_mirror([4096] * 32, 1, 64, 76, switch_pages=0)
+    assert flat["switch"] == 0 and len(flat["items"]) == 76 + 28
+
+
+def test_plan_switch_cost_dropped_when_steps_are_short():
+    """4096 one-page sequences over 76 ranges: a step of the line (~215 points)
+    exceeds the cost, so it applies; 3 one-page sequences over 3 ranges do not."""
+    assert plan_mirror([1] * 4096, 1, 4, 76)["switch"] == 3
+    pl = plan_mirror([1] * 3, 1, 4, 3)
+    assert pl["switch"] == 0 and len(pl["items"]) == 3
