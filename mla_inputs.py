@@ -236,6 +236,19 @@ def make_paged(inp: Inputs, *, perm_seed: int = 12345, spare_pages: int = 4,
     return Paged(cache=cache, block_table=bt, num_pages=num_pages, max_pages=max_pages, page_size=page)
 
 
+def latent_query_inputs(T: int, H: int, d_q: int, seed: int, d_nope: int = D_NOPE):
+    """Compressed query latents and the query up-projection for the query-side
+    absorption (seeded, numpy PCG64 ``default_rng(seed)``), in draw order:
+    c_q ~ N(0,1) [T, d_q], then w_uq ~ N(0,1) * (1/sqrt(d_q)) [d_q, H, d_nope]
+    (input-major: w_uq[k][h][i] maps compressed column k to head h's no-RoPE
+    query column i), float32 draws rounded to bf16. Returns (c_q, w_uq) bits."""
+    rng = np.random.default_rng(seed)
+    c_q = f32_to_bf16(rng.standard_normal((T, d_q), dtype=np.float32))
+    w_uq = f32_to_bf16((rng.standard_normal((d_q, H, d_nope), dtype=np.float32)
+                        * np.float32(1.0 / math.sqrt(d_q))).astype(np.float32))
+    return c_q, w_uq
+
+
 def workload_bytes(inp: Inputs) -> dict:
     """Algorithmic byte and flop counts of one decode step (cache read once)."""
     T, H = inp.T, inp.H

@@ -40,6 +40,10 @@ PINS = {
     "out_proj_f64": "pinned: numpy matmul; W_UV applied to absorbed_f64's u gives its out",
     "append_f64": "pinned: numpy matmul; the generator's rotation; identity weights; position 0; "
                   "norm and relative-position properties of the rotation",
+    "merge_w_kq_f64": "pinned: numpy per-head matmul; identity W_UQ gives W_UK; scores through the "
+                      "merged weight equal the explicit keys' scores",
+    "absorb_latent_f64": "pinned: equals absorb_q_f64 on the unmerged two-step query (associativity); "
+                         "zero and one-hot compressed queries",
 }
 
 
@@ -285,3 +289,43 @@ def append_f64(h_bits: np.ndarray, w_dkr_bits: np.ndarray, pos, theta: float = 1
     L.mla_oracle_append_f64(_p(h), _p(w), _p(p), T, d_model, d_c, D - d_c, float(theta), _p(out))
     return out
 
+
+
+def merge_w_kq_f64(w_uq_bits, w_uk_bits):
+    """Merged query weight per head: w_uq [d_q][H][d_nope] x w_uk [H][d_nope][d_c] ->
+    w_kq [d_q][H][d_c] (fp64), w_kq[k][h] = sum_i w_uq[k][h][i] w_uk[h][i]."""
+    L = _load()
+    wq = np.ascontiguousarray(w_uq_bits, dtype=np.uint16)
+    wk = np.ascontiguousarray(w_uk_bits, dtype=np.uint16)
+    d_q, H, d_nope = wq.shape
+    assert wk.shape[:2] == (H, d_nope)
+    d_c = wk.shape[2]
+    out = np.empty((d_q, H, d_c))
+    L.mla_oracle_merge_w_kq_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    L.mla_oracle_merge_w_kq_f64(_p(wq), _p(wk), d_q, H, d_nope, d_c, _p(out))
+    return out
+
+
+def absorb_latent_f64(c_q_bits, w_kq, q_rope_bits):
+    """Absorbed query from the compressed query latent: c_q [T][d_q] (bf16 bits) x
+    w_kq [d_q][H][d_c] (float64 values, or bf16 bits as uint16) -> [T][H][d_c + d_r],
+    the positional query q_rope [T][H][d_r] copied behind (fp64)."""
+    L = _load()
+    cq = np.ascontiguousarray(c_q_bits, dtype=np.uint16)
+    w = np.asarray(w_kq)
+    if w.dtype == np.uint16:
+        w = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    qr = np.ascontiguousarray(q_rope_bits, dtype=np.uint16)
+    T, d_q = cq.shape
+    assert w.shape[0] == d_q
+    H, d_c = w.shape[1], w.shape[2]
+    d_r = qr.shape[-1]
+    assert qr.shape == (T, H, d_r)
+    out = np.empty((T, H, d_c + d_r))
+    L.mla_oracle_absorb_latent_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_void_p]
+    L.mla_oracle_absorb_latent_f64(_p(cq), _p(w), _p(qr), T, H, d_q, d_r, d_c, _p(out))
+    return out

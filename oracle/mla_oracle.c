@@ -486,6 +486,52 @@ int mla_oracle_out_proj_f64(const uint16_t* u, const uint16_t* w_uv, int64_t T, 
     return 0;
 }
 
+/* ---------------------------------------------------------------- query-side absorption */
+/* The merged query weight (ingu627.github.io "Multi-Head Latent Attention (MLA)"
+ * section 2.2: S = C_KV^T (W_UK^T W_UQ) C_Q, read per head, since the softmax
+ * is taken per head). With the query up-projection stored input-major,
+ * w_uq[k][h][i] = weight from compressed-query column k to head h's no-RoPE
+ * query column i, and W_UK as w_uk[h][i][c]:
+ *   w_kq[k][h][c] = sum_i w_uq[k][h][i] * w_uk[h][i][c]
+ * so that sum_k c_q[k] w_kq[k][h][c] = sum_i (sum_k c_q[k] w_uq[k][h][i]) w_uk[h][i][c]. */
+int mla_oracle_merge_w_kq_f64(const uint16_t* w_uq, const uint16_t* w_uk, int d_q, int H, int d_nope,
+                              int d_c, double* w_kq) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < (int64_t)d_q * H; ++r) {
+        const int h = (int)(r % H);
+        const uint16_t* wk = w_uk + (int64_t)h * d_nope * d_c;
+        double* out = w_kq + r * d_c;
+        for (int cc = 0; cc < d_c; ++cc) out[cc] = 0.0;
+        for (int i = 0; i < d_nope; ++i) {
+            const double a = bf(w_uq[r * d_nope + i]);
+            for (int cc = 0; cc < d_c; ++cc) out[cc] += a * bf(wk[(int64_t)i * d_c + cc]);
+        }
+    }
+    return 0;
+}
+
+/* The absorbed query straight from the compressed query latent through the
+ * merged weight: q_abs[t][h][c] = sum_k c_q[t][k] w_kq[k][h][c] for c < d_c,
+ * then the (already rotated) positional query q^R[t][h] copied to columns
+ * d_c .. d_c + d_r - 1. w_kq is taken as given (fp64). */
+int mla_oracle_absorb_latent_f64(const uint16_t* c_q, const double* w_kq, const uint16_t* q_rope, int64_t T, int H,
+                                 int d_q, int d_r, int d_c, double* q_abs) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * H; ++r) {
+        const int64_t t = r / H;
+        const int h = (int)(r % H);
+        double* qa = q_abs + r * (d_c + d_r);
+        for (int cc = 0; cc < d_c; ++cc) qa[cc] = 0.0;
+        for (int k = 0; k < d_q; ++k) {
+            const double a = bf(c_q[t * d_q + k]);
+            const double* w = w_kq + ((int64_t)k * H + h) * d_c;
+            for (int cc = 0; cc < d_c; ++cc) qa[cc] += a * w[cc];
+        }
+        for (int e = 0; e < d_r; ++e) qa[d_c + e] = bf(q_rope[r * d_r + e]);
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- cache append */
 /* Latent-cache row of a new token (Huny section 1.2: c_t^KV = h_t W^DKV, the
  * joint low-rank compression; section 2.2: the decoupled positional key

@@ -284,3 +284,65 @@ def test_append_identity_weights_and_rotation_properties():
     d1 = r2[0, 512:] @ r2[1, 512:]
     d2 = r2[2, 512:] @ r2[3, 512:]
     assert abs(d1 - d2) < 1e-9 * max(1.0, abs(d1))
+
+
+# ------------------------------------------------------------------ query-side absorption
+def _latent_case(T=3, H=4, d_q=96, seed=9):
+    c_q, w_uq = mi.latent_query_inputs(T, H, d_q, seed)
+    rng = np.random.default_rng(seed + 1)
+    w_uk = mi.f32_to_bf16((rng.standard_normal((H, 128, 512)) / math.sqrt(512)).astype(np.float32))
+    q_rope = mi.f32_to_bf16(rng.standard_normal((T, H, 64)).astype(np.float32))
+    return c_q, w_uq, w_uk, q_rope
+
+
+def test_merged_weight_is_the_per_head_product():
+    """ingu627 "Multi-Head Latent Attention (MLA)" section 2.2, W_KQ = W_UK^T W_UQ per head,
+    against numpy's einsum; with W_UQ the identity (d_q = d_nope) the merge returns W_UK."""
+    _, w_uq, w_uk, _ = _latent_case()
+    m = oracle.merge_w_kq_f64(w_uq, w_uk)
+    assert np.abs(m - np.einsum("khi,hic->khc", f64(w_uq), f64(w_uk))).max() < 1e-12
+    H = w_uk.shape[0]
+    eye = np.zeros((128, H, 128), dtype=np.float32)
+    for h in range(H):
+        eye[:, h, :] = np.eye(128, dtype=np.float32)
+    m = oracle.merge_w_kq_f64(mi.f32_to_bf16(eye), w_uk)
+    assert np.array_equal(m, f64(w_uk).transpose(1, 0, 2))
+
+
+def test_latent_query_equals_the_two_step_query():
+    """Associativity: the absorbed query through the merged weight equals c_q W_UQ (the
+    no-RoPE query) followed by the absorption step of the unmerged path."""
+    c_q, w_uq, w_uk, q_rope = _latent_case()
+    qa = oracle.absorb_latent_f64(c_q, oracle.merge_w_kq_f64(w_uq, w_uk), q_rope)
+    q_nope = np.einsum("tk,khi->thi", f64(c_q), f64(w_uq))
+    two_step = np.einsum("thi,hic->thc", q_nope, f64(w_uk))
+    assert np.abs(qa[..., :512] - two_step).max() < 1e-12 * max(1.0, np.abs(two_step).max())
+    assert np.array_equal(qa[..., 512:], f64(q_rope))
+    # the same through the oracle's own absorption step, when q_nope is bf16-exact:
+    # one-hot compressed queries pick rows of W_UQ, which are bf16 values
+    T, d_q = c_q.shape
+    one_hot = np.zeros((T, d_q), dtype=np.float32)
+    ks = [0, d_q // 2, d_q - 1]
+    for t in range(T):
+        one_hot[t, ks[t]] = 1.0
+    oh = mi.f32_to_bf16(one_hot)
+    qa1 = oracle.absorb_latent_f64(oh, oracle.merge_w_kq_f64(w_uq, w_uk), q_rope)
+    ref = oracle.absorb_q_f64(np.stack([w_uq[k] for k in ks]), q_rope, w_uk)
+    assert np.abs(qa1 - ref).max() < 1e-12
+    zero = oracle.absorb_latent_f64(np.zeros_like(c_q), oracle.merge_w_kq_f64(w_uq, w_uk), q_rope)
+    assert not zero[..., :512].any() and np.array_equal(zero[..., 512:], f64(q_rope))
+
+
+def test_merged_scores_equal_the_explicit_keys_scores():
+    """S = C_KV^T (W_UK^T W_UQ) C_Q: the latent scores of the merged query equal the
+    scores of the explicitly reconstructed keys against the decompressed query."""
+    c_q, w_uq, w_uk, q_rope = _latent_case(T=2)
+    rng = np.random.default_rng(33)
+    c = mi.f32_to_bf16(rng.standard_normal((40, 512)).astype(np.float32))
+    qa = oracle.absorb_latent_f64(c_q, oracle.merge_w_kq_f64(w_uq, w_uk), q_rope)
+    q_nope = np.einsum("tk,khi->thi", f64(c_q), f64(w_uq))
+    for h in range(w_uk.shape[0]):
+        K = oracle.explicit_keys_f64(c, w_uk, h)  # [tokens][d_nope]
+        s_explicit = q_nope[:, h, :] @ K.T
+        s_latent = qa[:, h, :512] @ f64(c).T
+        assert np.abs(s_latent - s_explicit).max() < 1e-11 * max(1.0, np.abs(s_explicit).max())
