@@ -43,6 +43,7 @@ UNIT = "tokens/s"
 WORKLOAD_INDEX = 2
 NSETS = 3        # rotating input sets in the timed region
 D_MODEL = 7168   # hidden width of the cache-append phase (DeepSeek-V3)
+D_Q = 1536       # compressed query width of the query-side absorption line (DeepSeek-V3's; the pages leave it open)
 ROTATIONS = 10   # passes over the sets per graph replay
 
 
@@ -212,6 +213,8 @@ def run_ours(args):
     rng = np.random.default_rng(7168)
     h_bits = mi.f32_to_bf16(rng.standard_normal((T, D_MODEL)).astype(np.float32))
     w_dkr_bits = mi.f32_to_bf16((rng.standard_normal((576, D_MODEL)) / np.sqrt(D_MODEL)).astype(np.float32))
+    c_q_bits, w_uq_bits = mi.latent_query_inputs(T, H, D_Q, seed=1536)
+    w_uq_dev = to_dev(w_uq_bits)
     sets = []
     for _ in range(NSETS):
         sets.append(dict(
@@ -224,7 +227,10 @@ def run_ours(args):
             workspace=torch.empty(mla.workspace_bytes(B, n_q, H, G), dtype=torch.uint8, device=dev),
             u=torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
             lse=torch.empty((T, H), dtype=torch.float32, device=dev),
-            out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)))
+            out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev),
+            c_q=to_dev(c_q_bits)))
+        sets[-1]["w_kq"] = mla.merge_w_kq(w_uq_dev, sets[-1]["w_uk"])
+    del w_uq_dev
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -245,6 +251,9 @@ def run_ours(args):
     def append(S):  # the cache-append step (not part of the timed decode step)
         mla.append_kv(S["h"], S["w_dkr"], S["cache"], S["bt"], S["sl"], n_q=n_q, workspace=S["ws_app"],
                       err_word=err)
+
+    def absorb_latent(S):  # the query-side absorption through the merged W_KQ (not part of the timed step)
+        mla.absorb_q_latent(S["c_q"], S["q_rope"], S["w_kq"], S["q_abs"])
 
     def step(S):
         absorb(S)
@@ -326,6 +335,7 @@ def run_ours(args):
     phases = {"absorb_q": per_call_us(absorb), "decode_paged": per_call_us(decode),
               "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
     append_us = per_call_us(append)
+    latent_us = per_call_us(absorb_latent)
     # for reference: one step replayed alone after an L2 flush (cold caches,
     # including the graph launch, about 6.6 us on this system)
     g1 = capture(lambda: step(sets[0]))
@@ -403,6 +413,7 @@ def run_ours(args):
                          "duration": f"per call, {R} calls back to back over {NSETS} rotating input sets"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "append_kv": append_line(append_us, T, hbm),
+            "absorb_q_latent": latent_line(latent_us, phases["absorb_q"], T, H, hbm),
             "gpu_launches": 5 * args.steps,
             "timing": (f"CUDA events around the timed region: graphs of {R} back-to-back steps over "
                        f"{NSETS} rotating input sets, replayed until {args.steps} steps ran"),
@@ -423,6 +434,16 @@ def append_line(us, T, hbm):
     gbs = alg / (us * 1e-6) / 1e9
     return {"us": us, "d_model": D_MODEL, "rows": T, "alg_bytes": alg, "achieved_gbs": gbs, "peak_gbs": hbm,
             "frac": gbs / hbm, "bound": "hbm"}
+
+
+def latent_line(us, absorb_us, T, H, hbm):
+    """The query-side absorption through the merged weight (q_abs = c_q W_KQ, W_KQ = W_UQ W_UK per
+    head): its time per call and HBM roofline, beside the weight bytes of the unmerged route."""
+    alg = D_Q * H * 512 * 2 + T * D_Q * 2 + T * H * 64 * 2 + T * H * 576 * 2
+    gbs = alg / (us * 1e-6) / 1e9
+    return {"us": us, "d_q": D_Q, "rows": T, "heads": H, "alg_bytes": alg, "achieved_gbs": gbs, "peak_gbs": hbm,
+            "frac": gbs / hbm, "bound": "hbm", "merged_weight_bytes": D_Q * H * 512 * 2,
+            "unmerged_weight_bytes": D_Q * H * 128 * 2 + H * 128 * 512 * 2, "absorb_q_us": absorb_us}
 
 
 def stored_traffic():

@@ -9,6 +9,9 @@
  *                     partial softmax over page ranges, partial u = a C^KV (section 3.2)
  *   mla_combine       log-sum-exp merge of the range partials -> u, lse
  *   mla_out_proj      out = u W^UV per head                                (section 3.2)
+ * Beside the step: mla_append_kv writes the new tokens' cache rows, and
+ * mla_merge_w_kq / mla_absorb_q_latent give q_abs from the compressed query
+ * latent through the merged query-side weight.
  * One decode step for a batch is: mla_absorb_q -> mla_decode_paged ->
  * mla_combine -> mla_out_proj, all on one stream.
  *
@@ -88,6 +91,37 @@ size_t mla_page_bytes(int page_size, int d_c, int d_r);
  *   T >= 1 is the number of query rows (B * n_q). */
 mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
                         uint16_t* q_abs, int T, int H, int d_nope, int d_r, int d_c, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Query-side absorption through a merged weight (ingu627.github.io
+ * "Multi-Head Latent Attention (MLA)" section 2.2: S = C_KV^T (W_UK^T W_UQ) C_Q,
+ * W_KQ = W_UK^T W_UQ, taken per head because the softmax is per head).
+ *
+ * mla_merge_w_kq — the merge, done once per set of weights:
+ *   w_kq[k][h][c] = sum_i w_uq[k][h][i] * w_uk[h][i][c]
+ *   w_uq [d_q][H][d_nope] bf16, the query up-projection stored input-major
+ *        (w_uq[k][h][i] maps compressed-query column k to head h's no-RoPE
+ *        query column i), w_uk [H][d_nope][d_c] bf16,
+ *   w_kq [d_q][H][d_c] bf16 (output; fp32 accumulation, round-to-nearest-even).
+ *   64 <= d_q <= 16384, d_q % 64 == 0. w_uq and w_uk are read before the kernel
+ *   enqueued just before the call has finished.
+ *
+ * mla_absorb_q_latent — the absorbed query of each row straight from its
+ * compressed query latent, in place of mla_absorb_q (no separate W_UQ and
+ * W_UK products per step):
+ *   q_abs[t][h][c]       = sum_k c_q[t][k] * w_kq[k][h][c]    (c < d_c)
+ *   q_abs[t][h][d_c + e] = q_rope[t][h][e]                    (e < d_r)
+ *   c_q [T][d_q] bf16, w_kq [d_q][H][d_c] bf16 as written by mla_merge_w_kq,
+ *   q_rope [T][H][d_r] bf16 (already rotated), q_abs [T][H][d_c + d_r] bf16
+ *   (output). fp32 accumulation, bf16 (round-to-nearest-even) output. w_kq is
+ *   read before the kernel enqueued just before the call has finished; c_q and
+ *   q_rope after. At decode sizes the merged weight (d_q x H x d_c) is larger
+ *   than W_UQ and W_UK together when d_c > d_nope, so this trades bytes read
+ *   per step for one product instead of two. */
+mla_status mla_merge_w_kq(const uint16_t* w_uq, const uint16_t* w_uk, uint16_t* w_kq, int d_q, int H,
+                          int d_nope, int d_c, void* stream);
+mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, const uint16_t* w_kq,
+                               uint16_t* q_abs, int T, int H, int d_q, int d_r, int d_c, void* stream);
 
 /* ------------------------------------------------------------------------
  * Split-KV decode. The pages of all sequences, taken in sequence order, are

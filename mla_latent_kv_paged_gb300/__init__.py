@@ -44,6 +44,7 @@ EXPORTS = [
     "mla_decode_paged", "mla_combine", "mla_out_proj",
     "mla_decode_noalloc_max_bytes", "mla_decode_noalloc",
     "mla_append_workspace_bytes", "mla_append_kv",
+    "mla_merge_w_kq", "mla_absorb_q_latent",
 ]
 
 
@@ -97,6 +98,10 @@ def lib():
             L.mla_append_workspace_bytes.argtypes = [i, i]
             L.mla_append_kv.restype = i
             L.mla_append_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp]
+            L.mla_merge_w_kq.restype = i
+            L.mla_merge_w_kq.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.mla_absorb_q_latent.restype = i
+            L.mla_absorb_q_latent.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
             _lib = L
     return _lib
 
@@ -158,6 +163,31 @@ def absorb_q(q_nope, q_rope, w_uk, q_abs=None, stream=None):
                             _ptr(_bits(q_abs)), T, H, q_nope.shape[-1], q_rope.shape[-1],
                             w_uk.shape[-1], _stream(stream))
     _check(st, "mla_absorb_q")
+    return q_abs
+
+
+def merge_w_kq(w_uq, w_uk, w_kq=None, stream=None):
+    """Merged query-side weight: w_uq [d_q,H,128], w_uk [H,128,512] (bf16) -> w_kq [d_q,H,512]."""
+    import torch
+    d_q, H = w_uq.shape[0], w_uq.shape[1]
+    if w_kq is None:
+        w_kq = torch.empty((d_q, H, D_C), dtype=torch.bfloat16, device=w_uq.device)
+    st = lib().mla_merge_w_kq(_ptr(_bits(w_uq)), _ptr(_bits(w_uk)), _ptr(_bits(w_kq)), d_q, H, w_uq.shape[-1],
+                              w_uk.shape[-1], _stream(stream))
+    _check(st, "mla_merge_w_kq")
+    return w_kq
+
+
+def absorb_q_latent(c_q, q_rope, w_kq, q_abs=None, stream=None):
+    """c_q [T,d_q], q_rope [T,H,64], w_kq [d_q,H,512] (bf16) -> q_abs [T,H,576]."""
+    import torch
+    T, d_q = c_q.shape
+    H = w_kq.shape[1]
+    if q_abs is None:
+        q_abs = torch.empty((T, H, D_ROW), dtype=torch.bfloat16, device=c_q.device)
+    st = lib().mla_absorb_q_latent(_ptr(_bits(c_q)), _ptr(_bits(q_rope)), _ptr(_bits(w_kq)), _ptr(_bits(q_abs)),
+                                   T, H, d_q, q_rope.shape[-1], w_kq.shape[-1], _stream(stream))
+    _check(st, "mla_absorb_q_latent")
     return q_abs
 
 

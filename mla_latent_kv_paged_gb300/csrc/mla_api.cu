@@ -61,6 +61,25 @@ mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const ui
   return launch_status(launch_absorb_q(q_nope, q_rope, w_uk, q_abs, T, H, (cudaStream_t)stream));
 }
 
+mla_status mla_merge_w_kq(const uint16_t* w_uq, const uint16_t* w_uk, uint16_t* w_kq, int d_q, int H, int d_nope,
+                          int d_c, void* stream) {
+  if (!w_uq || !w_uk || !w_kq) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(w_uq) || !aligned16(w_uk) || !aligned16(w_kq)) return MLA_ERR_INVALID_ARG;
+  if (d_q < 1) return MLA_ERR_INVALID_ARG;
+  if (d_nope != kDNope || d_c != kDC || !heads_ok(H) || d_q % 64 != 0 || d_q > 16384)
+    return MLA_ERR_UNSUPPORTED_SHAPE;
+  return launch_status(launch_merge_w_kq(w_uq, w_uk, w_kq, d_q, H, (cudaStream_t)stream));
+}
+
+mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, const uint16_t* w_kq, uint16_t* q_abs,
+                               int T, int H, int d_q, int d_r, int d_c, void* stream) {
+  if (!c_q || !q_rope || !w_kq || !q_abs) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_q) || !aligned16(q_rope) || !aligned16(w_kq) || !aligned16(q_abs)) return MLA_ERR_INVALID_ARG;
+  if (T < 1 || d_q < 1) return MLA_ERR_INVALID_ARG;
+  if (d_r != kDR || d_c != kDC || !heads_ok(H) || d_q % 64 != 0 || d_q > 16384) return MLA_ERR_UNSUPPORTED_SHAPE;
+  return launch_status(launch_absorb_latent(c_q, q_rope, w_kq, q_abs, T, H, d_q, (cudaStream_t)stream));
+}
+
 int mla_decode_default_splits(int n_q) {
   if (n_q < 1) return -1;
   int dev = 0, sms = 0;

@@ -7,6 +7,10 @@
 //   D[c][t] = sum_i W_UK[h][i][c] q_nope[t][h][i]      M = 128 latent cols, N = rows t, K = 128
 //   A = W_UK[h][:, c-block] read M-major, B = q_nope rows (K-major).
 //   The rotated positional query is copied to columns 512..575.
+//   The same kernel merges the query-side weight (ingu627.github.io "Multi-Head
+//   Latent Attention (MLA)" section 2.2, W_KQ = W_UK^T W_UQ per head): the d_q
+//   rows of the input-major W_UQ [d_q][H][128] take the place of query rows,
+//   giving W_KQ [d_q][H][512] (rows of 512, no positional part).
 // out_proj (section 3.2, u W^UV):
 //   D[v][t] = sum_c W_UV[h][v][c] u[t][h][c]            M = 128 value cols, N = rows t, K = 512
 //   A = W_UV[h] (K-major), B = u rows (K-major). Each 64-wide K slice has its
@@ -44,7 +48,7 @@ template <bool kAbsorb, int kNT>
 __global__ void __launch_bounds__(kThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const uint16_t* __restrict__ weights, const uint16_t* __restrict__ q_rope, uint16_t* __restrict__ out,
-               int T, int H, int32_t* err_word) {
+               int T, int H, int out_row, int32_t* err_word) {
   using C = ProjCfg<kAbsorb, kNT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -134,11 +138,11 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     }
     // rotated positional query, copied unchanged next to the absorbed one, by
     // warps 1..3 while thread 0 waits for the tiles
-    if (kAbsorb && cblk == 0 && t0 == 0 && warp > 0) {
+    if (kAbsorb && q_rope && cblk == 0 && t0 == 0 && warp > 0) {
       for (int i = threadIdx.x - 32; i < T * (kDR / 8); i += kThreads - 32) {
         const int t = i / (kDR / 8), v = i % (kDR / 8);
         const uint4 w = reinterpret_cast<const uint4*>(q_rope + ((size_t)t * H + h) * kDR)[v];
-        reinterpret_cast<uint4*>(out + ((size_t)t * H + h) * kRow + kDC)[v] = w;
+        reinterpret_cast<uint4*>(out + ((size_t)t * H + h) * out_row + kDC)[v] = w;
       }
     }
     __syncwarp();
@@ -158,7 +162,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
         if (t < T) {
           const float f = __uint_as_float(r[v]);
           if (kAbsorb)
-            out[((size_t)t * H + h) * kRow + cblk * 128 + col] = float_to_bf16(f);
+            out[((size_t)t * H + h) * out_row + cblk * 128 + col] = float_to_bf16(f);
           else
             out[((size_t)t * H + h) * kDV + col] = float_to_bf16(f);
         }
@@ -178,7 +182,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
 
 template <bool kAbsorb, int kNT>
 cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint16_t* w, const uint16_t* q_rope,
-                        uint16_t* out, int T, int H, cudaStream_t s) {
+                        uint16_t* out, int T, int H, int out_row, cudaStream_t s) {
   using C = ProjCfg<kAbsorb, kNT>;
   static bool done = false;
   if (!done) {
@@ -189,7 +193,7 @@ cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint
   }
   const dim3 grid(H, kAbsorb ? kDC / 128 : 1);
   return launch_pdl(proj_tc_kernel<kAbsorb, kNT>, grid, dim3(kThreads), C::kSmem, s, ma, mb, w, q_rope, out, T,
-                    H, (int32_t*)nullptr);
+                    H, out_row, (int32_t*)nullptr);
 }
 
 bool maps(CUtensorMap* ma, CUtensorMap* mb, const uint16_t* w, const uint16_t* act, int T, int H, int K, int nt) {
@@ -202,14 +206,26 @@ bool maps(CUtensorMap* ma, CUtensorMap* mb, const uint16_t* w, const uint16_t* a
 
 }  // namespace
 
-cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
-                            uint16_t* q_abs, int T, int H, cudaStream_t s) {
+namespace {
+cudaError_t absorb_rows(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk, uint16_t* out, int T,
+                        int H, int out_row, cudaStream_t s) {
   const int nt = T <= 32 ? 32 : T <= 64 ? 64 : 128;
   CUtensorMap ma, mb;
   if (!maps(&ma, &mb, w_uk, q_nope, T, H, kDNope, nt)) return cudaErrorInvalidValue;
-  if (nt == 32) return launch_proj<true, 32>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
-  if (nt == 64) return launch_proj<true, 64>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
-  return launch_proj<true, 128>(ma, mb, w_uk, q_rope, q_abs, T, H, s);
+  if (nt == 32) return launch_proj<true, 32>(ma, mb, w_uk, q_rope, out, T, H, out_row, s);
+  if (nt == 64) return launch_proj<true, 64>(ma, mb, w_uk, q_rope, out, T, H, out_row, s);
+  return launch_proj<true, 128>(ma, mb, w_uk, q_rope, out, T, H, out_row, s);
+}
+}  // namespace
+
+cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const uint16_t* w_uk,
+                            uint16_t* q_abs, int T, int H, cudaStream_t s) {
+  return absorb_rows(q_nope, q_rope, w_uk, q_abs, T, H, kRow, s);
+}
+
+cudaError_t launch_merge_w_kq(const uint16_t* w_uq, const uint16_t* w_uk, uint16_t* w_kq, int d_q, int H,
+                              cudaStream_t s) {
+  return absorb_rows(w_uq, nullptr, w_uk, w_kq, d_q, H, kDC, s);
 }
 
 cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
@@ -217,8 +233,8 @@ cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* o
   const int nt = T <= 32 ? 32 : 64;
   CUtensorMap ma, mb;
   if (!maps(&ma, &mb, w_uv, u, T, H, kDC, nt)) return cudaErrorInvalidValue;
-  if (nt == 32) return launch_proj<false, 32>(ma, mb, w_uv, nullptr, out, T, H, s);
-  return launch_proj<false, 64>(ma, mb, w_uv, nullptr, out, T, H, s);
+  if (nt == 32) return launch_proj<false, 32>(ma, mb, w_uv, nullptr, out, T, H, kDV, s);
+  return launch_proj<false, 64>(ma, mb, w_uv, nullptr, out, T, H, kDV, s);
 }
 
 }  // namespace mla

@@ -157,6 +157,27 @@ def test_host_validation_append(lib):
     assert app(wsb=ws - 1) == 3
 
 
+def test_host_validation_query_side_absorption(lib):
+    p = FAKE
+
+    def merge(**kw):
+        a = dict(wq=p, wk=p, out=p, d_q=1536, H=128, dn=128, dc=512)
+        a.update(kw)
+        return lib.mla_merge_w_kq(a["wq"], a["wk"], a["out"], a["d_q"], a["H"], a["dn"], a["dc"], None)
+
+    def latent(**kw):
+        a = dict(cq=p, qr=p, w=p, out=p, T=32, H=128, d_q=1536, dr=64, dc=512)
+        a.update(kw)
+        return lib.mla_absorb_q_latent(a["cq"], a["qr"], a["w"], a["out"], a["T"], a["H"], a["d_q"], a["dr"],
+                                       a["dc"], None)
+
+    assert merge(wq=None) == 1 and merge(out=p + 8) == 1 and merge(d_q=0) == 1
+    assert merge(d_q=100) == 2 and merge(d_q=16384 + 64) == 2 and merge(H=129) == 2
+    assert merge(dn=64) == 2 and merge(dc=256) == 2
+    assert latent(qr=None) == 1 and latent(cq=p + 2) == 1 and latent(T=0) == 1
+    assert latent(d_q=96) == 2 and latent(dr=32) == 2 and latent(dc=576) == 2 and latent(H=0) == 2
+
+
 @pytest.mark.parametrize("lens,G", [([256, 256], 76), ([4096] * 32, 76), ([64] * 3, 2),
                                     ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5),
                                     ([4096] * 32, 38), ([64] * 500, 76), ([1] * 4096, 76),
