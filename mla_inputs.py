@@ -249,6 +249,15 @@ def latent_query_inputs(T: int, H: int, d_q: int, seed: int, d_nope: int = D_NOP
     return c_q, w_uq
 
 
+def output_projection(d_model: int, H: int, seed: int, d_v: int = D_V):
+    """The attention output projection W^O, one row per output column, w_o[n][h][v]
+    ~ N(0,1) * (1/sqrt(H * d_v)) [d_model, H, d_v] (float32 draws rounded to bf16,
+    numpy PCG64 ``default_rng(seed)``). Returns bf16 bits."""
+    rng = np.random.default_rng(seed)
+    w = rng.standard_normal((d_model, H, d_v), dtype=np.float32) * np.float32(1.0 / math.sqrt(H * d_v))
+    return f32_to_bf16(w.astype(np.float32))
+
+
 def workload_bytes(inp: Inputs) -> dict:
     """Algorithmic byte and flop counts of one decode step (cache read once)."""
     T, H = inp.T, inp.H

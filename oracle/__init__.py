@@ -44,6 +44,9 @@ PINS = {
                       "merged weight equal the explicit keys' scores",
     "absorb_latent_f64": "pinned: equals absorb_q_f64 on the unmerged two-step query (associativity); "
                          "zero and one-hot compressed queries",
+    "merge_w_comb_f64": "pinned: numpy per-head product; an identity output projection gives W_UV",
+    "out_comb_f64": "pinned: equals out_proj_f64 followed by the output projection (associativity); "
+                    "identity output projection gives out_proj_f64's heads side by side",
 }
 
 
@@ -328,4 +331,39 @@ def absorb_latent_f64(c_q_bits, w_kq, q_rope_bits):
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_void_p]
     L.mla_oracle_absorb_latent_f64(_p(cq), _p(w), _p(qr), T, H, d_q, d_r, d_c, _p(out))
+    return out
+
+
+def merge_w_comb_f64(w_uv_bits, w_o_bits):
+    """Merged value/output weight per head: w_uv [H][d_v][d_c] x w_o [d_model][H][d_v] ->
+    w_comb [d_model][H][d_c] (fp64), w_comb[n][h] = sum_v w_o[n][h][v] w_uv[h][v]."""
+    L = _load()
+    wv = np.ascontiguousarray(w_uv_bits, dtype=np.uint16)
+    wo = np.ascontiguousarray(w_o_bits, dtype=np.uint16)
+    H, d_v, d_c = wv.shape
+    d_model = wo.shape[0]
+    assert wo.shape == (d_model, H, d_v)
+    out = np.empty((d_model, H, d_c))
+    L.mla_oracle_merge_w_comb_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    L.mla_oracle_merge_w_comb_f64(_p(wv), _p(wo), H, d_v, d_c, d_model, _p(out))
+    return out
+
+
+def out_comb_f64(u_bits, w_comb):
+    """Layer output through the merged weight: u [T][H][d_c] (bf16 bits) and w_comb
+    [d_model][H][d_c] (float64 values, or bf16 bits as uint16) -> out [T][d_model] (fp64)."""
+    L = _load()
+    u = np.ascontiguousarray(u_bits, dtype=np.uint16)
+    w = np.asarray(w_comb)
+    if w.dtype == np.uint16:
+        w = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    T, H, d_c = u.shape
+    d_model = w.shape[0]
+    assert w.shape == (d_model, H, d_c)
+    out = np.empty((T, d_model))
+    L.mla_oracle_out_comb_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    L.mla_oracle_out_comb_f64(_p(u), _p(w), T, H, d_c, d_model, _p(out))
     return out

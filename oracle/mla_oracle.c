@@ -532,6 +532,47 @@ int mla_oracle_absorb_latent_f64(const uint16_t* c_q, const double* w_kq, const 
     return 0;
 }
 
+/* ---------------------------------------------------------------- merged output projection */
+/* The merged value/output weight (Huny's Dev Blog "MLA 아키텍처 해부" section
+ * 3, item 2: HeadOut_i = (a_i C^KV)(W_i^UV W_i^O), W_i,comb = W_i^UV W_i^O of
+ * size d_c x d; ikmyungterran.us, the absorbed W~^O = W^UV W^O). With W^UV
+ * stored as w_uv[h][v][c] (value column v of head h from latent column c) and
+ * the output projection one row per output column, w_o[n][h][v]:
+ *   w_comb[n][h][c] = sum_v w_o[n][h][v] * w_uv[h][v][c]. */
+int mla_oracle_merge_w_comb_f64(const uint16_t* w_uv, const uint16_t* w_o, int H, int d_v, int d_c, int d_model,
+                                double* w_comb) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < (int64_t)d_model * H; ++r) {
+        const int h = (int)(r % H);
+        const uint16_t* wv = w_uv + (int64_t)h * d_v * d_c;
+        double* out = w_comb + r * d_c;
+        for (int cc = 0; cc < d_c; ++cc) out[cc] = 0.0;
+        for (int v = 0; v < d_v; ++v) {
+            const double a = bf(w_o[r * d_v + v]);
+            for (int cc = 0; cc < d_c; ++cc) out[cc] += a * bf(wv[(int64_t)v * d_c + cc]);
+        }
+    }
+    return 0;
+}
+
+/* The attention layer's output through the merged weight, summed over the
+ * heads (the output projection of the concatenated heads):
+ *   out[t][n] = sum_h sum_c u[t][h][c] * w_comb[n][h][c]. w_comb is taken as given (fp64). */
+int mla_oracle_out_comb_f64(const uint16_t* u, const double* w_comb, int64_t T, int H, int d_c, int d_model,
+                            double* out) {
+    const int64_t K = (int64_t)H * d_c;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < T * d_model; ++r) {
+        const int64_t t = r / d_model, n = r % d_model;
+        const uint16_t* ut = u + t * K;
+        const double* w = w_comb + n * K;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) acc += bf(ut[k]) * w[k];
+        out[r] = acc;
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- cache append */
 /* Latent-cache row of a new token (Huny section 1.2: c_t^KV = h_t W^DKV, the
  * joint low-rank compression; section 2.2: the decoupled positional key

@@ -346,3 +346,39 @@ def test_merged_scores_equal_the_explicit_keys_scores():
         s_explicit = q_nope[:, h, :] @ K.T
         s_latent = qa[:, h, :512] @ f64(c).T
         assert np.abs(s_latent - s_explicit).max() < 1e-11 * max(1.0, np.abs(s_explicit).max())
+
+
+# ------------------------------------------------------------------ merged output projection
+def _comb_case(T=3, H=4, d_model=80, seed=13):
+    rng = np.random.default_rng(seed)
+    u = mi.f32_to_bf16((rng.standard_normal((T, H, 512)) * 0.3).astype(np.float32))
+    w_uv = mi.f32_to_bf16((rng.standard_normal((H, 128, 512)) / math.sqrt(512)).astype(np.float32))
+    w_o = mi.output_projection(d_model, H, seed + 1)
+    return u, w_uv, w_o
+
+
+def test_merged_output_weight_is_the_per_head_product():
+    """Huny section 3 item 2, W_i,comb = W_i^UV W_i^O, against numpy's einsum; an identity
+    output projection (d_model = H * d_v) gives W_UV itself."""
+    u, w_uv, w_o = _comb_case()
+    m = oracle.merge_w_comb_f64(w_uv, w_o)
+    assert np.abs(m - np.einsum("nhv,hvc->nhc", f64(w_o), f64(w_uv))).max() < 1e-12
+    H = w_uv.shape[0]
+    eye = np.eye(H * 128, dtype=np.float32).reshape(H * 128, H, 128)
+    m = oracle.merge_w_comb_f64(w_uv, mi.f32_to_bf16(eye))
+    assert np.array_equal(m.reshape(H, 128, H, 512)[np.arange(H), :, np.arange(H)], f64(w_uv))
+
+
+def test_merged_output_equals_out_proj_then_output_projection():
+    """Associativity: u W_comb summed over heads equals the unmerged route, the per-head
+    up-projection (the oracle's out_proj) followed by the output projection."""
+    u, w_uv, w_o = _comb_case()
+    got = oracle.out_comb_f64(u, oracle.merge_w_comb_f64(w_uv, w_o))
+    heads = oracle.out_proj_f64(u, w_uv)  # [T][H][d_v]
+    ref = np.einsum("thv,nhv->tn", heads, f64(w_o))
+    assert np.abs(got - ref).max() < 1e-12 * max(1.0, np.abs(ref).max())
+    # identity output projection: the heads side by side
+    H = w_uv.shape[0]
+    eye = mi.f32_to_bf16(np.eye(H * 128, dtype=np.float32).reshape(H * 128, H, 128))
+    side = oracle.out_comb_f64(u, oracle.merge_w_comb_f64(w_uv, eye))
+    assert np.abs(side - heads.reshape(u.shape[0], -1)).max() < 1e-12
