@@ -215,6 +215,7 @@ def run_ours(args):
     w_dkr_bits = mi.f32_to_bf16((rng.standard_normal((576, D_MODEL)) / np.sqrt(D_MODEL)).astype(np.float32))
     c_q_bits, w_uq_bits = mi.latent_query_inputs(T, H, D_Q, seed=1536)
     w_uq_dev = to_dev(w_uq_bits)
+    w_o_dev = to_dev(mi.output_projection(D_MODEL, H, seed=7169))
     sets = []
     for _ in range(NSETS):
         sets.append(dict(
@@ -230,7 +231,10 @@ def run_ours(args):
             out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev),
             c_q=to_dev(c_q_bits)))
         sets[-1]["w_kq"] = mla.merge_w_kq(w_uq_dev, sets[-1]["w_uk"])
-    del w_uq_dev
+        sets[-1]["w_comb"] = mla.merge_w_comb(sets[-1]["w_uv"], w_o_dev)
+        sets[-1]["ws_comb"] = torch.empty(mla.out_comb_workspace_bytes(T, H, D_MODEL), dtype=torch.uint8, device=dev)
+        sets[-1]["out_model"] = torch.empty((T, D_MODEL), dtype=torch.bfloat16, device=dev)
+    del w_uq_dev, w_o_dev
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -254,6 +258,9 @@ def run_ours(args):
 
     def absorb_latent(S):  # the query-side absorption through the merged W_KQ (not part of the timed step)
         mla.absorb_q_latent(S["c_q"], S["q_rope"], S["w_kq"], S["q_abs"])
+
+    def out_comb(S):  # the layer output through the merged W_comb (not part of the timed step)
+        mla.out_comb(S["u"], S["w_comb"], S["out_model"], workspace=S["ws_comb"])
 
     def step(S):
         absorb(S)
@@ -336,6 +343,7 @@ def run_ours(args):
               "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
     append_us = per_call_us(append)
     latent_us = per_call_us(absorb_latent)
+    comb_us = per_call_us(out_comb)
     # for reference: one step replayed alone after an L2 flush (cold caches,
     # including the graph launch, about 6.6 us on this system)
     g1 = capture(lambda: step(sets[0]))
@@ -414,6 +422,7 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "append_kv": append_line(append_us, T, hbm),
             "absorb_q_latent": latent_line(latent_us, phases["absorb_q"], T, H, hbm),
+            "out_comb": comb_line(comb_us, phases["out_proj"], T, H, hbm),
             "gpu_launches": 5 * args.steps,
             "timing": (f"CUDA events around the timed region: graphs of {R} back-to-back steps over "
                        f"{NSETS} rotating input sets, replayed until {args.steps} steps ran"),
@@ -444,6 +453,17 @@ def latent_line(us, absorb_us, T, H, hbm):
     return {"us": us, "d_q": D_Q, "rows": T, "heads": H, "alg_bytes": alg, "achieved_gbs": gbs, "peak_gbs": hbm,
             "frac": gbs / hbm, "bound": "hbm", "merged_weight_bytes": D_Q * H * 512 * 2,
             "unmerged_weight_bytes": D_Q * H * 128 * 2 + H * 128 * 512 * 2, "absorb_q_us": absorb_us}
+
+
+def comb_line(us, out_proj_us, T, H, hbm):
+    """The layer output through the merged value/output weight (out = sum_h u_h W_comb,h, W_comb =
+    W_UV W_O per head): its time per call and HBM roofline, beside the weight bytes of the unmerged
+    route (out_proj, then the output projection)."""
+    alg = D_MODEL * H * 512 * 2 + T * H * 512 * 2 + T * D_MODEL * 2
+    gbs = alg / (us * 1e-6) / 1e9
+    return {"us": us, "d_model": D_MODEL, "rows": T, "heads": H, "alg_bytes": alg, "achieved_gbs": gbs,
+            "peak_gbs": hbm, "frac": gbs / hbm, "bound": "hbm", "merged_weight_bytes": D_MODEL * H * 512 * 2,
+            "unmerged_weight_bytes": H * 128 * 512 * 2 + D_MODEL * H * 128 * 2, "out_proj_us": out_proj_us}
 
 
 def stored_traffic():

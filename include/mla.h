@@ -9,9 +9,11 @@
  *                     partial softmax over page ranges, partial u = a C^KV (section 3.2)
  *   mla_combine       log-sum-exp merge of the range partials -> u, lse
  *   mla_out_proj      out = u W^UV per head                                (section 3.2)
- * Beside the step: mla_append_kv writes the new tokens' cache rows, and
+ * Beside the step: mla_append_kv writes the new tokens' cache rows,
  * mla_merge_w_kq / mla_absorb_q_latent give q_abs from the compressed query
- * latent through the merged query-side weight.
+ * latent through the merged query-side weight, and mla_merge_w_comb /
+ * mla_out_comb give the layer output from u through the merged value/output
+ * weight.
  * One decode step for a batch is: mla_absorb_q -> mla_decode_paged ->
  * mla_combine -> mla_out_proj, all on one stream.
  *
@@ -118,6 +120,41 @@ mla_status mla_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope, const ui
  *   q_rope after. At decode sizes the merged weight (d_q x H x d_c) is larger
  *   than W_UQ and W_UK together when d_c > d_nope, so this trades bytes read
  *   per step for one product instead of two. */
+/* ------------------------------------------------------------------------
+ * Merged value/output projection (Huny's Dev Blog "MLA 아키텍처 해부" section 3,
+ * item 2: HeadOut_i = (a_i C^KV)(W_i^UV W_i^O), W_i,comb = W_i^UV W_i^O;
+ * ikmyungterran.us, W~^O = W^UV W^O). The layer output is the sum of the heads'
+ * outputs (the output projection of the concatenated heads).
+ *
+ * mla_merge_w_comb — the merge, done once per set of weights:
+ *   w_comb[n][h][c] = sum_v w_o[n][h][v] * w_uv[h][v][c]
+ *   w_uv [H][d_v][d_c] bf16 (as for mla_out_proj), w_o [d_model][H][d_v] bf16,
+ *   the output projection with one row per output column, w_comb
+ *   [d_model][H][d_c] bf16 (output; fp32 accumulation, round-to-nearest-even).
+ *   d_model % 128 == 0, 128 <= d_model <= 65536. w_uv and w_o are read before
+ *   the kernel enqueued just before the call has finished.
+ *
+ * mla_out_comb — the layer output straight from the merged latent outputs u,
+ * in place of mla_out_proj followed by the output projection:
+ *   out[t][n] = sum_h sum_c u[t][h][c] * w_comb[n][h][c]
+ *   u [T][H][d_c] bf16 (mla_combine's output), w_comb as written by
+ *   mla_merge_w_comb, out [T][d_model] bf16. The reduction over H * d_c is split
+ *   across CTAs into fp32 partials in `workspace` (>= mla_out_comb_workspace_bytes
+ *   bytes, no initial contents needed, 16-byte aligned) that a second kernel
+ *   adds in a fixed order: results are bit-reproducible. 1 <= T <= 2 *
+ *   MLA_MAX_BATCH. w_comb is read before the kernel enqueued just before the
+ *   call has finished; u after. The merged weight (d_model x H x d_c) is
+ *   d_c / d_v = 4 times the output projection's bytes, so at decode sizes the
+ *   merge trades bytes read per step for one product instead of two.
+ *
+ * mla_out_comb_workspace_bytes: bytes of workspace for these sizes (0 if they
+ * are invalid). */
+mla_status mla_merge_w_comb(const uint16_t* w_uv, const uint16_t* w_o, uint16_t* w_comb, int H, int d_v, int d_c,
+                            int d_model, void* stream);
+size_t mla_out_comb_workspace_bytes(int T, int H, int d_model);
+mla_status mla_out_comb(const uint16_t* u, const uint16_t* w_comb, uint16_t* out, int T, int H, int d_c,
+                        int d_model, void* workspace, size_t workspace_bytes, void* stream);
+
 mla_status mla_merge_w_kq(const uint16_t* w_uq, const uint16_t* w_uk, uint16_t* w_kq, int d_q, int H,
                           int d_nope, int d_c, void* stream);
 mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, const uint16_t* w_kq,

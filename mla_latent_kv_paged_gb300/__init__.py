@@ -45,6 +45,7 @@ EXPORTS = [
     "mla_decode_noalloc_max_bytes", "mla_decode_noalloc",
     "mla_append_workspace_bytes", "mla_append_kv",
     "mla_merge_w_kq", "mla_absorb_q_latent",
+    "mla_merge_w_comb", "mla_out_comb_workspace_bytes", "mla_out_comb",
 ]
 
 
@@ -102,6 +103,12 @@ def lib():
             L.mla_merge_w_kq.argtypes = [vp, vp, vp, i, i, i, i, vp]
             L.mla_absorb_q_latent.restype = i
             L.mla_absorb_q_latent.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+            L.mla_merge_w_comb.restype = i
+            L.mla_merge_w_comb.argtypes = [vp, vp, vp, i, i, i, i, vp]
+            L.mla_out_comb_workspace_bytes.restype = sz
+            L.mla_out_comb_workspace_bytes.argtypes = [i, i, i]
+            L.mla_out_comb.restype = i
+            L.mla_out_comb.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
             _lib = L
     return _lib
 
@@ -189,6 +196,41 @@ def absorb_q_latent(c_q, q_rope, w_kq, q_abs=None, stream=None):
                                    T, H, d_q, q_rope.shape[-1], w_kq.shape[-1], _stream(stream))
     _check(st, "mla_absorb_q_latent")
     return q_abs
+
+
+def merge_w_comb(w_uv, w_o, w_comb=None, stream=None):
+    """Merged value/output weight: w_uv [H,128,512], w_o [d_model,H,128] (bf16) -> w_comb [d_model,H,512]."""
+    import torch
+    H = w_uv.shape[0]
+    d_model = w_o.shape[0]
+    if w_comb is None:
+        w_comb = torch.empty((d_model, H, D_C), dtype=torch.bfloat16, device=w_uv.device)
+    st = lib().mla_merge_w_comb(_ptr(_bits(w_uv)), _ptr(_bits(w_o)), _ptr(_bits(w_comb)), H, w_uv.shape[1],
+                                w_uv.shape[2], d_model, _stream(stream))
+    _check(st, "mla_merge_w_comb")
+    return w_comb
+
+
+def out_comb_workspace_bytes(T: int, H: int, d_model: int) -> int:
+    n = int(lib().mla_out_comb_workspace_bytes(T, H, d_model))
+    if n == 0:
+        raise MlaError(1, "mla_out_comb_workspace_bytes")
+    return n
+
+
+def out_comb(u, w_comb, out=None, *, workspace=None, stream=None):
+    """u [T,H,512], w_comb [d_model,H,512] (bf16) -> out [T,d_model], the layer output."""
+    import torch
+    T, H = u.shape[0], u.shape[1]
+    d_model = w_comb.shape[0]
+    if out is None:
+        out = torch.empty((T, d_model), dtype=torch.bfloat16, device=u.device)
+    if workspace is None:
+        workspace = torch.empty(out_comb_workspace_bytes(T, H, d_model), dtype=torch.uint8, device=u.device)
+    st = lib().mla_out_comb(_ptr(_bits(u)), _ptr(_bits(w_comb)), _ptr(_bits(out)), T, H, u.shape[-1], d_model,
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "mla_out_comb")
+    return out
 
 
 def decode_paged(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,

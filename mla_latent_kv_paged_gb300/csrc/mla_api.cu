@@ -80,6 +80,36 @@ mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, cons
   return launch_status(launch_absorb_latent(c_q, q_rope, w_kq, q_abs, T, H, d_q, (cudaStream_t)stream));
 }
 
+namespace {
+bool comb_shape_ok(int H, int d_model) { return heads_ok(H) && d_model % 128 == 0 && d_model >= 128 && d_model <= 65536; }
+}  // namespace
+
+mla_status mla_merge_w_comb(const uint16_t* w_uv, const uint16_t* w_o, uint16_t* w_comb, int H, int d_v, int d_c,
+                            int d_model, void* stream) {
+  if (!w_uv || !w_o || !w_comb) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(w_uv) || !aligned16(w_o) || !aligned16(w_comb)) return MLA_ERR_INVALID_ARG;
+  if (d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (d_v != kDV || d_c != kDC || !comb_shape_ok(H, d_model)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  // w_comb[n][h][c] = sum_v w_o[n][h][v] w_uv[h][v][c]: the absorption kernel with
+  // the rows of w_o in place of query rows and w_uv in place of w_uk
+  return launch_status(launch_merge_w_kq(w_o, w_uv, w_comb, d_model, H, (cudaStream_t)stream));
+}
+
+size_t mla_out_comb_workspace_bytes(int T, int H, int d_model) {
+  if (T < 1 || T > 2 * MLA_MAX_BATCH || !comb_shape_ok(H, d_model)) return 0;
+  return out_comb_workspace_bytes(T, H, d_model);
+}
+
+mla_status mla_out_comb(const uint16_t* u, const uint16_t* w_comb, uint16_t* out, int T, int H, int d_c, int d_model,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!u || !w_comb || !out || !workspace) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(w_comb) || !aligned16(out) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  if (T < 1 || d_model < 1) return MLA_ERR_INVALID_ARG;
+  if (T > 2 * MLA_MAX_BATCH || d_c != kDC || !comb_shape_ok(H, d_model)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < out_comb_workspace_bytes(T, H, d_model)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  return launch_status(launch_out_comb(u, w_comb, out, T, H, d_model, workspace, (cudaStream_t)stream));
+}
+
 int mla_decode_default_splits(int n_q) {
   if (n_q < 1) return -1;
   int dev = 0, sms = 0;

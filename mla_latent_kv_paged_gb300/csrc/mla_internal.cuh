@@ -132,6 +132,9 @@ cudaError_t launch_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* o
                             cudaStream_t s);
 cudaError_t launch_merge_w_kq(const uint16_t* w_uq, const uint16_t* w_uk, uint16_t* w_kq, int d_q, int H,
                               cudaStream_t s);
+size_t out_comb_workspace_bytes(int T, int H, int d_model);
+cudaError_t launch_out_comb(const uint16_t* u, const uint16_t* w_comb, uint16_t* out, int T, int H, int d_model,
+                            void* workspace, cudaStream_t s);
 cudaError_t launch_absorb_latent(const uint16_t* c_q, const uint16_t* q_rope, const uint16_t* w_kq, uint16_t* q_abs,
                                  int T, int H, int d_q, cudaStream_t s);
 size_t append_workspace_bytes(int T, int d_model);

@@ -178,6 +178,31 @@ def test_host_validation_query_side_absorption(lib):
     assert latent(d_q=96) == 2 and latent(dr=32) == 2 and latent(dc=576) == 2 and latent(H=0) == 2
 
 
+def test_host_validation_merged_output_projection(lib):
+    p = FAKE
+    ws = lib.mla_out_comb_workspace_bytes(32, 128, 7168)
+    assert ws == 32 * 7168 * 4 * (304 // 56)  # one row tile, five splits of fp32 partials
+    assert lib.mla_out_comb_workspace_bytes(0, 128, 7168) == 0
+    assert lib.mla_out_comb_workspace_bytes(32, 128, 7100) == 0
+    assert lib.mla_out_comb_workspace_bytes(32, 129, 7168) == 0
+
+    def merge(**kw):
+        a = dict(wv=p, wo=p, out=p, H=128, dv=128, dc=512, d=7168)
+        a.update(kw)
+        return lib.mla_merge_w_comb(a["wv"], a["wo"], a["out"], a["H"], a["dv"], a["dc"], a["d"], None)
+
+    def comb(**kw):
+        a = dict(u=p, w=p, out=p, T=32, H=128, dc=512, d=7168, ws=p, wsb=ws)
+        a.update(kw)
+        return lib.mla_out_comb(a["u"], a["w"], a["out"], a["T"], a["H"], a["dc"], a["d"], a["ws"], a["wsb"], None)
+
+    assert merge(wo=None) == 1 and merge(out=p + 4) == 1 and merge(d=0) == 1
+    assert merge(d=7100) == 2 and merge(dv=64) == 2 and merge(dc=576) == 2 and merge(H=0) == 2
+    assert comb(ws=None) == 1 and comb(u=p + 2) == 1 and comb(T=0) == 1
+    assert comb(T=2 * 4096 + 1) == 2 and comb(d=64) == 2 and comb(dc=256) == 2
+    assert comb(wsb=ws - 1) == 3
+
+
 @pytest.mark.parametrize("lens,G", [([256, 256], 76), ([4096] * 32, 76), ([64] * 3, 2),
                                     ([1, 65, 130, 64, 5000], 7), ([100], 1), ([7, 9], 5),
                                     ([4096] * 32, 38), ([64] * 500, 76), ([1] * 4096, 76),
