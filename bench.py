@@ -275,6 +275,18 @@ def run_ours(args):
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
+    if args.profile_phase:  # one side call alone, eagerly (short profiling runs)
+        fn = {"absorb_q_latent": absorb_latent, "out_comb": out_comb, "append_kv": append}[args.profile_phase]
+        for k in range(6):
+            fn(sets[k % NSETS])
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise SystemExit(f"device error word {int(err.item())}")
+        if rank == 0:
+            print(json.dumps({"profile_phase": args.profile_phase, "calls": 6}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -499,6 +511,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="time the steps only (no phase times, end-to-end leg or CPU baseline): for profiling runs")
+    ap.add_argument("--profile-phase", choices=["absorb_q_latent", "out_comb", "append_kv"], default=None,
+                    help="after the warm-up, run this call 6 times over the rotating sets and stop: for profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
