@@ -148,26 +148,39 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
     __syncwarp();
     if (!wait_phase(bar_d, phase, abort_flag, err_word)) break;
     tc_fence_after();
-    // epilogue: lane = output column, registers = rows t
+    // epilogue: lane = output column, registers = rows t. The tile goes through
+    // shared memory (the B operand's space, free once the MMAs are done) as
+    // [rows][128 columns] bf16, so that each output row leaves as 16-byte stores
+    // of 256 contiguous bytes (one 2-byte store per column and row had queued
+    // for microseconds)
     const int col = warp * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tile = sbase + C::kOffB;
 #pragma unroll 1
     for (int c0 = 0; c0 < C::NT; c0 += 32) {
       uint32_t r[32];
       tmem_ld32(taddr + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int v = 0; v < 32; ++v) {
-        const int t = t0 + c0 + v;
-        if (t < T) {
-          const float f = __uint_as_float(r[v]);
-          if (kAbsorb)
-            out[((size_t)t * H + h) * out_row + cblk * 128 + col] = float_to_bf16(f);
-          else
-            out[((size_t)t * H + h) * kDV + col] = float_to_bf16(f);
-        }
+      for (int v = 0; v < 32; ++v)
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(tile + (uint32_t)(c0 + v) * 256u + 2u * col),
+                     "h"(float_to_bf16(__uint_as_float(r[v])))
+                     : "memory");
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < C::NT * 16; i += kThreads) {
+      const int row = i >> 4, part = i & 15, t = t0 + row;
+      if (t < T) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(tile + (uint32_t)row * 256u + 16u * part));
+        uint16_t* dst = kAbsorb ? out + ((size_t)t * H + h) * out_row + cblk * 128
+                                : out + ((size_t)t * H + h) * kDV;
+        reinterpret_cast<uint4*>(dst)[part] = v;
       }
     }
+    fence_proxy_async_smem();  // the next rows' B tile is written by TMA
     tc_fence_before();
     __syncthreads();  // D and the B tile are free for the next rows
     tc_fence_after();
