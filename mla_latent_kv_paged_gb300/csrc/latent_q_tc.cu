@@ -33,6 +33,7 @@ struct LatentCfg {
   static constexpr uint32_t kSmem = kOffBar + 8 * (2 * kStages + 1) + 16;
   static constexpr uint32_t kTmCols = kNT;
   static_assert(kStage % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(kNT * 256 <= kStage, "the epilogue tile fits the first stage");
 };
 
 template <int kNT>
@@ -135,8 +136,10 @@ absorb_latent_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_con
     __syncwarp();
     if (!wait_phase(bar_d, dphase, abort_flag, nullptr)) break;
     tc_fence_after();
-    // epilogue: lane = output column, registers = rows t
-    const int col = cblk * 128 + warp * 32 + lane;
+    // epilogue: lane = output column, registers = rows t. The tile goes through
+    // shared memory (the first ring stage: every MMA of the tile is done) as
+    // [rows][128 columns] bf16, and each row leaves as 16-byte stores
+    const int col = warp * 32 + lane;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
     for (int c0 = 0; c0 < kNT; c0 += 32) {
@@ -144,13 +147,25 @@ absorb_latent_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_con
       tmem_ld32(taddr + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int v = 0; v < 32; ++v) {
-        const int t = t0 + c0 + v;
-        if (t < T) q_abs[((size_t)t * H + h) * kRow + col] = float_to_bf16(__uint_as_float(r[v]));
+      for (int v = 0; v < 32; ++v)
+        asm volatile("st.shared.u16 [%0], %1;" ::"r"(sbase + (uint32_t)(c0 + v) * 256u + 2u * col),
+                     "h"(float_to_bf16(__uint_as_float(r[v])))
+                     : "memory");
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kNT * 16; i += kThreads) {
+      const int row = i >> 4, part = i & 15, t = t0 + row;
+      if (t < T) {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(sbase + (uint32_t)row * 256u + 16u * part));
+        reinterpret_cast<uint4*>(q_abs + ((size_t)t * H + h) * kRow + cblk * 128)[part] = v;
       }
     }
+    fence_proxy_async_smem();  // the ring stages are written by TMA again for the next rows
     tc_fence_before();
-    __syncthreads();  // D is free for the next rows
+    __syncthreads();  // D and the first stage are free for the next rows
     tc_fence_after();
   }
   tc_fence_before();
