@@ -8,7 +8,7 @@
 // Blog "MLA 아키텍처 해부" section 4 table names FlashDecoding / PagedAttention
 // as the decode techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
 //
-// One block of 1024 threads. Integer work only; the output is a pure function
+// One block of 256 threads. Integer work only; the output is a pure function
 // of (seq_lens, n_q, max_pages, G), so repeated calls give identical plans.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
@@ -16,7 +16,8 @@
 namespace mla {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;  // barriers of a smaller block are cheaper; the work is light
+constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kSwitchPages = 3;
 
 // Exclusive scan of v[0..n) in place (shared memory), returns the total.
@@ -38,17 +39,17 @@ __device__ int block_exclusive_scan(int* v, int n, int* warp_sums) {
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < kPlanWarps ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    warp_sums[lane] = w;  // inclusive over warps
+    if (lane < kPlanWarps) warp_sums[lane] = w;  // inclusive over warps
   }
   __syncthreads();
   int excl = x - local + (warp > 0 ? warp_sums[warp - 1] : 0);
-  const int total = warp_sums[31];
+  const int total = warp_sums[kPlanWarps - 1];
   for (int i = lo; i < hi; ++i) {
     int t = v[i];
     v[i] = excl;
@@ -58,7 +59,13 @@ __device__ int block_exclusive_scan(int* v, int n, int* warp_sums) {
   return total;
 }
 
-__device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// a / b for a >= 0, b > 0: a 32-bit division when both fit (always at serving
+// sizes), a 64-bit one otherwise; the same quotient either way
+__device__ inline int64_t div_nn(int64_t a, int64_t b) {
+  if (((uint64_t)a | (uint64_t)b) >> 32 == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
+}
+__device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return div_nn(a + b - 1, b); }
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table, int B,
@@ -97,7 +104,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   // step along the line would not exceed it: steps of at least a+1 keep two
   // cuts from landing on the same sequence start, so no range is empty.
   const int64_t V0 = (int64_t)total + (int64_t)kSwitchPages * (B - 1);
-  const int64_t a = (V0 / Ge >= kSwitchPages + 1) ? kSwitchPages : 0;
+  const int64_t a = (div_nn(V0, Ge) >= kSwitchPages + 1) ? kSwitchPages : 0;
   const int64_t V = (int64_t)total + a * (B - 1);
 
   // 2. pieces per sequence: cuts strictly inside (Q_b, Q_b + n_b)
@@ -129,7 +136,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     int k = s_istart[b];
     int64_t start = Pb;
     for (int64_t p = lo; p <= hi; ++p) {
-      const int64_t x = (p * V) / Ge - a * b;  // global page of the cut
+      const int64_t x = div_nn(p * V, Ge) - a * b;  // global page of the cut
       plan.item_seq[k] = b;
       plan.item_page0[k] = (int)(start - Pb);
       plan.item_page1[k] = (int)(x - Pb);
@@ -151,7 +158,7 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     } else if (p >= Ge) {
       r = s_items;
     } else {
-      const int64_t x = ((int64_t)p * V) / Ge;
+      const int64_t x = div_nn((int64_t)p * V, Ge);
       // largest b whose stretch of the line (switch, then pages) starts at or
       // before x: Q_b - a <= x for b >= 1 (strictly increasing in b)
       int lo = 0, hi = B - 1;
