@@ -35,8 +35,8 @@
  *     still finishing (programmatic dependent launch): mla_absorb_q and
  *     mla_out_proj load their weights (w_uk, w_uv) in that time, so weights
  *     must not be written by the kernel enqueued just before the call. Every
- *     other input is read after that kernel has finished (and see
- *     mla_decode_paged for its own rule).
+ *     other input is read after that kernel has finished, except seq_lens
+ *     and the workspace of mla_decode_paged (see its ordering rule).
  *   - Errors that only the device can see (a context length out of range, a
  *     page id outside [0, num_pages), a wait that timed out) are written as
  *     the first nonzero mla_status into *err_word (a device int32 the caller
@@ -222,7 +222,13 @@ size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);
  *   block_table [B][max_pages_per_seq] int32 physical page ids
  *   seq_lens    [B] int32, n_q <= L <= max_pages_per_seq * page_size
  *   workspace   >= mla_decode_workspace_bytes(B, n_q, H, num_splits) bytes
- *   err_word    device int32 or NULL (see the conventions above). */
+ *   err_word    device int32 or NULL (see the conventions above).
+ * Ordering: the split plan is computed while the kernel enqueued just before
+ * the call is still finishing (in the step, mla_absorb_q): seq_lens is read
+ * and the plan arrays of workspace are written in that time, so that kernel
+ * must neither write seq_lens nor use workspace (for example an mla_combine
+ * of an earlier call on the same workspace). q_abs, cache and block_table are
+ * read after it has finished. */
 mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                             const int32_t* block_table, const int32_t* seq_lens,
                             int B, int n_q, int H, int num_pages, int page_size,

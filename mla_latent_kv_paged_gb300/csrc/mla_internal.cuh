@@ -116,9 +116,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // ---------------------------------------------------------------- launchers
+// overlap: start beside the kernel enqueued before (programmatic dependent
+// launch); it then reads seq_lens and writes the plan while that kernel runs.
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
                         int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
-                        cudaStream_t s);
+                        cudaStream_t s, bool overlap = true);
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
                           int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s);

@@ -85,8 +85,10 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache, cons
   Plan plan;
   plan_layout(scratch, B, n_q, H, num_splits, &plan);
   cudaStream_t s = (cudaStream_t)stream;
+  // the plan waits for the kernel before it: that may be the previous call's
+  // merge, still reading the plan in the shared array
   cudaError_t e = launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
-                              err_word, s);
+                              err_word, s, /*overlap=*/false);
   if (e == cudaSuccess)
     e = launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, max_pages_per_seq, softmax_scale,
                       num_splits, plan, err_word, s);

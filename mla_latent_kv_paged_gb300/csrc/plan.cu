@@ -190,15 +190,19 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
                         int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool overlap) {
   const size_t smem = (size_t)2 * (B + 1) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, block_table, B, n_q, max_pages,
-                    num_pages, G, plan, err_word);
+  if (overlap)
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, block_table, B, n_q, max_pages,
+                      num_pages, G, plan, err_word);
+  // after the previous kernel has finished (its grid dependency wait then returns at once)
+  plan_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, block_table, B, n_q, max_pages, num_pages, G, plan, err_word);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import mla_inputs as mi
-from tests.helpers import MAX_ABS, MEAN_REL, assert_close, dev_bf16_to_f64, device_inputs
+from tests.helpers import MAX_ABS, MEAN_REL, assert_close, dev_bf16_to_f64, dev_to_bits, device_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -63,3 +63,33 @@ def test_noalloc_refuses_requests_beyond_its_array():
     p = ctypes.c_void_p(x.data_ptr())
     st = lib.mla_decode_noalloc(p, p, p, p, B, n_q, H, 8, 64, 4, ctypes.c_float(0.07), G, p, p, None, None)
     assert st == 3  # MLA_ERR_WORKSPACE_TOO_SMALL, nothing launched
+
+
+def test_noalloc_back_to_back_calls_with_different_lengths():
+    """Calls enqueued back to back share the library's array: the second call's plan (other
+    lengths, so other pieces) must not overwrite the array while the first call's merge still
+    reads it. Each call is compared bit for bit with the workspace entry point."""
+    import torch
+
+    import mla_latent_kv_paged_gb300 as mla
+    mla.build()
+    H = 128
+    inps = [mi.make_inputs(B=8, H=H, n_q=1, seq_lens=lens, seed=70 + i)
+            for i, lens in enumerate([[4096] * 8, [64, 5000, 1, 700, 3000, 130, 2000, 900]])]
+    pgs = [mi.make_paged(x, spare_pages=2) for x in inps]
+    ds = [device_inputs(x, pg) for x, pg in zip(inps, pgs)]
+    q_abs = [mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"]) for d in ds]
+    refs = []
+    for i, d in enumerate(ds):
+        ws, G = mla.decode_paged(q_abs[i], d["cache"], d["block_table"], d["seq_lens"], n_q=1, num_splits=20)
+        refs.append(mla.combine(ws, B=8, n_q=1, H=H, num_splits=G))
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(4):  # the two calls back to back, several times
+        for i, d in enumerate(ds):
+            outs.append((i, mla.decode_noalloc(q_abs[i], d["cache"], d["block_table"], d["seq_lens"], n_q=1,
+                                               num_splits=20)))
+    torch.cuda.synchronize()
+    for i, (u, lse) in outs:
+        assert np.array_equal(dev_to_bits(u), dev_to_bits(refs[i][0]))
+        assert np.array_equal(lse.cpu().numpy().view(np.uint32), refs[i][1].cpu().numpy().view(np.uint32))
