@@ -2,9 +2,10 @@
 
 Default workload: DeepSeek-V3-shaped decode, B=32 sequences x context 4096,
 H=128 heads, page 64, one query token per sequence (seeded synthetic data,
-random weights). One step = mla_absorb_q -> mla_decode_paged -> mla_combine
--> mla_out_proj for the whole batch; tokens/s = query tokens per step / step
-time. Steps run back to back (CUDA graphs of consecutive steps) over three
+random weights). One step = mla_decode_plan -> mla_absorb_q ->
+mla_decode_paged_planned -> mla_combine -> mla_out_proj for the whole batch
+(the split plan is computed beside the previous kernel); tokens/s = query
+tokens per step / step time. Steps run back to back (CUDA graphs of consecutive steps) over three
 complete input sets at distinct addresses used in rotation, so every step reads
 inputs that are no longer in L2 (the sets together are ~4.5x the L2); the timed
 region is bracketed by CUDA events on the launching stream. The JSON line also
@@ -242,9 +243,17 @@ def run_ours(args):
     def absorb(S):
         mla.absorb_q(S["q_nope"], S["q_rope"], S["w_uk"], S["q_abs"])
 
-    def decode(S):
+    def decode(S):  # the plan and the split-KV decode kernel in one call
         mla.decode_paged(S["q_abs"], S["cache"], S["bt"], S["sl"], n_q=n_q, num_splits=G,
                          workspace=S["workspace"], err_word=err)
+
+    def plan(S):  # the split plan alone (in the step: enqueued before absorb_q)
+        mla.decode_plan(S["sl"], n_q=n_q, H=H, max_pages=pg.max_pages, num_pages=pg.num_pages, num_splits=G,
+                        workspace=S["workspace"], err_word=err)
+
+    def decode_planned(S):  # the split-KV decode kernel alone, on the workspace's plan
+        mla.decode_paged(S["q_abs"], S["cache"], S["bt"], S["sl"], n_q=n_q, num_splits=G,
+                         workspace=S["workspace"], err_word=err, planned=True)
 
     def combine(S):
         mla.combine(S["workspace"], B=B, n_q=n_q, H=H, num_splits=G, u=S["u"], lse=S["lse"])
@@ -263,8 +272,9 @@ def run_ours(args):
         mla.out_comb(S["u"], S["w_comb"], S["out_model"], workspace=S["ws_comb"])
 
     def step(S):
+        plan(S)
         absorb(S)
-        decode(S)
+        decode_planned(S)
         combine(S)
         out_proj(S)
 
@@ -351,8 +361,13 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return
-    phases = {"absorb_q": per_call_us(absorb), "decode_paged": per_call_us(decode),
-              "combine": per_call_us(combine), "out_proj": per_call_us(out_proj)}
+    for k in range(NSETS):  # every set's workspace holds its plan for the planned decode calls
+        plan(sets[k])
+    phases = {"decode_plan": per_call_us(plan), "absorb_q": per_call_us(absorb),
+              "decode_paged_planned": per_call_us(decode_planned), "combine": per_call_us(combine),
+              "out_proj": per_call_us(out_proj),
+              # for reference: the plan and the decode kernel in one call
+              "decode_paged": per_call_us(decode)}
     append_us = per_call_us(append)
     latent_us = per_call_us(absorb_latent)
     comb_us = per_call_us(out_comb)
@@ -413,7 +428,7 @@ def run_ours(args):
     if rank == 0:
         hbm, tflops, src = peaks()
         wb = mi.workload_bytes(inp)
-        dec_us = phases["decode_paged"]
+        dec_us = phases["decode_paged_planned"]
         dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
         achieved = dec_bytes / (dec_us * 1e-6) / 1e9
         traffic = stored_traffic()
@@ -424,7 +439,7 @@ def run_ours(args):
             "config": workload_config(inp, G),
             "phases_us": phases,
             "single_step_flushed_us": float(np.median(single)),
-            "roofline": {"kernel": "mla_decode_paged (plan + split-KV decode kernels)", "bound": "hbm",
+            "roofline": {"kernel": "mla_decode_paged_planned (the split-KV decode kernel)", "bound": "hbm",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": src,
                          "alg_bytes_per_launch": dec_bytes, "alg_flops_per_launch": wb["decode_flops"],
@@ -496,7 +511,7 @@ def mla_kernel_rev():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_latent_kv_paged_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(("decode", "plan")) or name.endswith(".cuh"):
+        if name.startswith("decode") or name.endswith(".cuh"):
             h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 

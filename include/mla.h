@@ -15,7 +15,9 @@
  * mla_out_comb give the layer output from u through the merged value/output
  * weight.
  * One decode step for a batch is: mla_absorb_q -> mla_decode_paged ->
- * mla_combine -> mla_out_proj, all on one stream.
+ * mla_combine -> mla_out_proj, all on one stream (or, with the split plan
+ * computed ahead: mla_decode_plan -> mla_absorb_q -> mla_decode_paged_planned
+ * -> mla_combine -> mla_out_proj).
  *
  * Conventions shared by every call:
  *   - All tensor pointers are DEVICE pointers, owned and allocated by the
@@ -235,6 +237,23 @@ mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                             int max_pages_per_seq, float softmax_scale, int num_splits,
                             void* workspace, size_t workspace_bytes, int32_t* err_word,
                             void* stream);
+
+/* mla_decode_plan + mla_decode_paged_planned — mla_decode_paged in two calls,
+ * so that the split plan can be computed earlier in the step: enqueue
+ * mla_decode_plan before mla_absorb_q (it then runs beside the kernel before
+ * it, under the same ordering rule for seq_lens and workspace), and
+ * mla_decode_paged_planned where mla_decode_paged would go. The planned call
+ * launches only the decode kernel and reads the plan that mla_decode_plan
+ * wrote into workspace for the same B, n_q, H, max_pages_per_seq and
+ * num_splits (and the seq_lens it was given); results are bit-identical to
+ * mla_decode_paged. Arguments as for mla_decode_paged. */
+mla_status mla_decode_plan(const int32_t* seq_lens, int B, int n_q, int H, int num_pages, int page_size,
+                           int max_pages_per_seq, int num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* err_word, void* stream);
+mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
+                                    int B, int n_q, int H, int num_pages, int page_size, int max_pages_per_seq,
+                                    float softmax_scale, int num_splits, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_word, void* stream);
 
 /* mla_combine — merge the range partials of each (sequence, query, head):
  *   lse = ln sum_k exp(lse_k),  u = sum_k exp(lse_k - lse) * o_k

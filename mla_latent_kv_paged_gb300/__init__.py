@@ -41,7 +41,7 @@ STATUS = {
 EXPORTS = [
     "mla_status_string", "mla_abi_version", "mla_cache_bytes_per_token", "mla_page_bytes",
     "mla_absorb_q", "mla_decode_default_splits", "mla_decode_workspace_bytes",
-    "mla_decode_paged", "mla_combine", "mla_out_proj",
+    "mla_decode_paged", "mla_decode_plan", "mla_decode_paged_planned", "mla_combine", "mla_out_proj",
     "mla_decode_noalloc_max_bytes", "mla_decode_noalloc",
     "mla_append_workspace_bytes", "mla_append_kv",
     "mla_merge_w_kq", "mla_absorb_q_latent",
@@ -88,6 +88,10 @@ def lib():
             L.mla_decode_workspace_bytes.argtypes = [i, i, i, i]
             L.mla_decode_paged.restype = i
             L.mla_decode_paged.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
+            L.mla_decode_plan.restype = i
+            L.mla_decode_plan.argtypes = [vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
+            L.mla_decode_paged_planned.restype = i
+            L.mla_decode_paged_planned.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
             L.mla_combine.restype = i
             L.mla_combine.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.mla_out_proj.restype = i
@@ -233,8 +237,26 @@ def out_comb(u, w_comb, out=None, *, workspace=None, stream=None):
     return out
 
 
+def decode_plan(seq_lens, *, n_q: int, H: int, max_pages: int, num_pages: int, num_splits: int | None = None,
+                workspace=None, err_word=None, stream=None):
+    """The split plan alone, into ``workspace`` (allocated if None). Returns (workspace,
+    num_splits); pass both to ``decode_paged(..., planned=True)``."""
+    import torch
+    B = seq_lens.shape[0]
+    if num_splits is None:
+        num_splits = default_splits(n_q)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(B, n_q, H, num_splits), dtype=torch.uint8, device=seq_lens.device)
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    st = lib().mla_decode_plan(_ptr(seq_lens), B, n_q, H, num_pages, PAGE, max_pages, num_splits, _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
+    _check(st, "mla_decode_plan")
+    return workspace, num_splits
+
+
 def decode_paged(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
-                 softmax_scale: float = DEFAULT_SCALE, workspace=None, err_word=None, stream=None):
+                 softmax_scale: float = DEFAULT_SCALE, workspace=None, err_word=None, stream=None,
+                 planned: bool = False):
     """Split-KV decode over the paged cache. Returns (workspace, num_splits).
 
     q_abs [B*n_q, H, 576] (or [B, n_q, H, 576]), cache [num_pages, 64, 576],
@@ -251,8 +273,15 @@ def decode_paged(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: i
     need = workspace_bytes(B, n_q, H, num_splits)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q_abs.device)
-    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
-    assert block_table.is_contiguous() and seq_lens.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.is_contiguous()
+    if planned:  # the workspace holds the plan written by decode_plan
+        st = lib().mla_decode_paged_planned(_ptr(_bits(q_abs)), _ptr(_bits(cache)), _ptr(block_table), B, n_q, H,
+                                            num_pages, page_size, max_pages, float(softmax_scale), num_splits,
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            _ptr(err_word), _stream(stream))
+        _check(st, "mla_decode_paged_planned")
+        return workspace, num_splits
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
     st = lib().mla_decode_paged(_ptr(_bits(q_abs)), _ptr(_bits(cache)), _ptr(block_table),
                                 _ptr(seq_lens), B, n_q, H, num_pages, page_size, max_pages,
                                 float(softmax_scale), num_splits, _ptr(workspace),
@@ -348,18 +377,20 @@ def out_proj(u, w_uv, out=None, stream=None):
 def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int,
                 num_splits: int | None = None, softmax_scale: float = DEFAULT_SCALE,
                 bufs: dict | None = None, err_word=None, stream=None):
-    """One full decode step: absorb_q -> decode_paged -> combine -> out_proj.
+    """One full decode step: decode_plan -> absorb_q -> decode_paged (planned) ->
+    combine -> out_proj (the plan is computed beside the kernel before it).
 
     ``bufs`` may hold preallocated q_abs, workspace, u, lse, out tensors.
     Returns dict(q_abs, u, lse, out).
     """
     bufs = bufs or {}
-    B = block_table.shape[0]
+    B, max_pages = block_table.shape
     T, H = q_nope.shape[0], q_nope.shape[1]
+    ws, g = decode_plan(seq_lens, n_q=n_q, H=H, max_pages=max_pages, num_pages=cache.shape[0],
+                        num_splits=num_splits, workspace=bufs.get("workspace"), err_word=err_word, stream=stream)
     q_abs = absorb_q(q_nope, q_rope, w_uk, bufs.get("q_abs"), stream)
-    ws, g = decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=num_splits,
-                         softmax_scale=softmax_scale, workspace=bufs.get("workspace"),
-                         err_word=err_word, stream=stream)
+    decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=g, softmax_scale=softmax_scale,
+                 workspace=ws, err_word=err_word, stream=stream, planned=True)
     u, lse = combine(ws, B=B, n_q=n_q, H=H, num_splits=g, u=bufs.get("u"), lse=bufs.get("lse"),
                      stream=stream)
     out = out_proj(u, w_uv, bufs.get("out"), stream)
@@ -367,8 +398,8 @@ def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q
 
 
 class CapturedStep:
-    """A whole decode step (absorb_q -> decode_paged -> combine -> out_proj)
-    captured once in a CUDA graph, for serving loops with fixed shapes.
+    """A whole decode step (decode_plan -> absorb_q -> decode_paged -> combine ->
+    out_proj) captured once in a CUDA graph, for serving loops with fixed shapes.
 
     The step owns its query, workspace and output buffers; it keeps pointers to
     the caller's weights, cache, block_table and seq_lens, so changing their

@@ -133,32 +133,70 @@ size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits) {
   return plan_layout(nullptr, B, n_q, H, num_splits, nullptr);
 }
 
-mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
-                            const int32_t* block_table, const int32_t* seq_lens,
-                            int B, int n_q, int H, int num_pages, int page_size,
-                            int max_pages_per_seq, float softmax_scale, int num_splits,
-                            void* workspace, size_t workspace_bytes, int32_t* err_word,
-                            void* stream) {
-  if (!q_abs || !cache || !block_table || !seq_lens || !workspace) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(block_table) || !aligned16(seq_lens) ||
-      !aligned16(workspace))
-    return MLA_ERR_INVALID_ARG;
+namespace {
+// the checks shared by the decode entry points; fills `plan` on success
+mla_status decode_args(void* workspace, size_t workspace_bytes, int B, int n_q, int H, int num_pages,
+                       int page_size, int max_pages_per_seq, int num_splits, Plan* plan) {
+  if (!workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   if (B < 1 || num_pages < 1 || max_pages_per_seq < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
   if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H) || page_size != kPage)
     return MLA_ERR_UNSUPPORTED_SHAPE;
   if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
     return MLA_ERR_UNSUPPORTED_SHAPE;
   const size_t need = plan_layout(nullptr, B, n_q, H, num_splits, nullptr);
   if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  plan_layout(workspace, B, n_q, H, num_splits, plan);
+  return MLA_OK;
+}
+}  // namespace
+
+mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
+                            const int32_t* block_table, const int32_t* seq_lens,
+                            int B, int n_q, int H, int num_pages, int page_size,
+                            int max_pages_per_seq, float softmax_scale, int num_splits,
+                            void* workspace, size_t workspace_bytes, int32_t* err_word,
+                            void* stream) {
+  if (!q_abs || !cache || !block_table || !seq_lens) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(block_table) || !aligned16(seq_lens))
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
   Plan plan;
-  plan_layout(workspace, B, n_q, H, num_splits, &plan);
+  mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
+                              num_splits, &plan);
+  if (st != MLA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  mla_status st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq,
-                                            num_pages, num_splits, plan, err_word, s));
+  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
+                                 err_word, s));
   if (st != MLA_OK) return st;
   return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages,
                                      max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
+}
+
+mla_status mla_decode_plan(const int32_t* seq_lens, int B, int n_q, int H, int num_pages, int page_size,
+                           int max_pages_per_seq, int num_splits, void* workspace, size_t workspace_bytes,
+                           int32_t* err_word, void* stream) {
+  if (!seq_lens || !aligned16(seq_lens)) return MLA_ERR_INVALID_ARG;
+  Plan plan;
+  mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
+                              num_splits, &plan);
+  if (st != MLA_OK) return st;
+  return launch_status(launch_plan(seq_lens, nullptr, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
+                                   err_word, (cudaStream_t)stream));
+}
+
+mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
+                                    int B, int n_q, int H, int num_pages, int page_size, int max_pages_per_seq,
+                                    float softmax_scale, int num_splits, void* workspace, size_t workspace_bytes,
+                                    int32_t* err_word, void* stream) {
+  if (!q_abs || !cache || !block_table) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(block_table)) return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
+  Plan plan;
+  mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
+                              num_splits, &plan);
+  if (st != MLA_OK) return st;
+  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, max_pages_per_seq,
+                                     softmax_scale, num_splits, plan, err_word, (cudaStream_t)stream));
 }
 
 mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_splits, uint16_t* u,

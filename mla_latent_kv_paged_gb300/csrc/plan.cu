@@ -76,6 +76,9 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   __shared__ int warp_sums[32];
   __shared__ int s_items;
   const int tid = threadIdx.x;
+  // the next kernel may start at once: it reads the plan only after its own
+  // grid dependency wait, which covers this kernel's completion
+  sm100::grid_launch_dependents();
 
   // 1. clamp context lengths, count pages
   for (int b = tid; b < B; b += kPlanThreads) {
@@ -179,10 +182,9 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   }
 
   // Page ids are checked by the decode kernel when it reads them. The plan
-  // does not read anything the previous kernel wrote, so it may run beside
-  // it; it waits for that kernel only before finishing, so the decode kernel
-  // that waits for the plan also sees everything written before it.
-  sm100::grid_launch_dependents();
+  // does not read anything the previous kernel wrote, so it runs beside it;
+  // it waits for that kernel only before finishing, so a kernel that waits
+  // for the plan also sees everything written before it.
   sm100::grid_dependency_wait();
 }
 

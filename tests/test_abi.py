@@ -131,6 +131,32 @@ def test_host_validation_decode_and_combine(lib):
     assert lib.mla_combine(p, 2, 1, 16, 4, p + 4, p, None) == 1
 
 
+def test_host_validation_plan_and_planned_decode(lib):
+    p = FAKE
+    ws = lib.mla_decode_workspace_bytes(2, 1, 16, 4)
+
+    def plan(**kw):
+        a = dict(sl=p, B=2, n_q=1, H=16, num_pages=8, page=64, maxp=4, G=4, ws=p, wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_decode_plan(a["sl"], a["B"], a["n_q"], a["H"], a["num_pages"], a["page"], a["maxp"], a["G"],
+                                   a["ws"], a["wsb"], a["err"], None)
+
+    def dec(**kw):
+        a = dict(q=p, cache=p, bt=p, B=2, n_q=1, H=16, num_pages=8, page=64, maxp=4, scale=0.07, G=4, ws=p,
+                 wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_decode_paged_planned(a["q"], a["cache"], a["bt"], a["B"], a["n_q"], a["H"], a["num_pages"],
+                                            a["page"], a["maxp"], a["scale"], a["G"], a["ws"], a["wsb"], a["err"],
+                                            None)
+
+    assert plan(sl=None) == 1 and plan(sl=p + 4) == 1 and plan(ws=None) == 1 and plan(B=0) == 1
+    assert plan(G=0) == 1 and plan(n_q=3) == 2 and plan(page=128) == 2 and plan(H=129) == 2
+    assert plan(wsb=ws - 1) == 3
+    assert dec(q=None) == 1 and dec(bt=p + 4) == 1 and dec(scale=0.0) == 1 and dec(ws=p + 8) == 1
+    assert dec(n_q=0) == 2
+    assert dec(page=32) == 2 and dec(wsb=ws - 1) == 3
+
+
 def test_host_validation_append(lib):
     p = FAKE
     ws = lib.mla_append_workspace_bytes(2, 512)

@@ -363,3 +363,38 @@ def test_full_size_workload_sampled(mla, index):
     # every row is finite
     assert np.isfinite(dev_bf16_to_f64(r["out"])).all()
     assert np.isfinite(r["lse"].cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("case", ["tiny", "ragged_multitoken", "many_short"])
+def test_planned_decode_equals_decode_paged(mla, case):
+    """mla_decode_plan (enqueued before mla_absorb_q) then mla_decode_paged_planned gives the
+    workspace plan and the merged u, lse of mla_decode_paged bit for bit."""
+    import torch
+    splits = None
+    if case == "tiny":
+        inp = mi.workload_inputs(1)
+    elif case == "ragged_multitoken":
+        inp = mi.make_inputs(B=9, H=16, n_q=2, seq_lens=[2, 3, 64, 65, 129, 500, 1000, 77, 4000], seed=5)
+        splits = 7
+    else:
+        lens = np.random.default_rng(7).integers(1, 131, size=1000)
+        inp = mi.make_inputs(B=1000, H=8, n_q=1, seq_lens=list(lens), seed=7)
+    pg = mi.make_paged(inp, spare_pages=2)
+    d = device_inputs(inp, pg)
+    B, H = inp.B, inp.H
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_abs = mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"])
+    ws1, g = mla.decode_paged(q_abs, d["cache"], d["block_table"], d["seq_lens"], n_q=inp.n_q,
+                              num_splits=splits, err_word=err)
+    u1, lse1 = mla.combine(ws1, B=B, n_q=inp.n_q, H=H, num_splits=g)
+    ws2, g2 = mla.decode_plan(d["seq_lens"], n_q=inp.n_q, H=H, max_pages=pg.max_pages, num_pages=pg.num_pages,
+                              num_splits=g, err_word=err)
+    q2 = mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"])
+    mla.decode_paged(q2, d["cache"], d["block_table"], d["seq_lens"], n_q=inp.n_q, num_splits=g2, workspace=ws2,
+                     err_word=err, planned=True)
+    u2, lse2 = mla.combine(ws2, B=B, n_q=inp.n_q, H=H, num_splits=g2)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and g2 == g
+    assert np.array_equal(ws1[:12].cpu().numpy(), ws2[:12].cpu().numpy())  # pieces, used splits, pages
+    assert np.array_equal(dev_to_bits(u1), dev_to_bits(u2))
+    assert np.array_equal(lse1.cpu().numpy().view(np.uint32), lse2.cpu().numpy().view(np.uint32))
