@@ -145,7 +145,7 @@ def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return
-    inp = mi.workload_inputs(WORKLOAD_INDEX)
+    inp = mi.workload_inputs(args.workload)
     T = inp.B * inp.n_q
     per_step = max(1, min(inp.B, 4))
     times = []
@@ -176,9 +176,13 @@ def run_reference(args):
 
 
 def workload_config(inp, num_splits):
-    return {"workload": f"DeepSeek-V3-shaped MLA decode: B={inp.B} x context "
-                        f"{int(inp.seq_lens[0])}, H={inp.H}, d_c=512, d_r=64, page 64, n_q={inp.n_q}",
-            "batch": inp.B, "context": int(inp.seq_lens[0]), "heads": inp.H, "n_q": inp.n_q,
+    lens = inp.seq_lens
+    ctx = (f"context {int(lens[0])}" if (lens == lens[0]).all()
+           else f"contexts {int(lens.min())}..{int(lens.max())} (mean {float(lens.mean()):.0f})")
+    return {"workload": f"DeepSeek-V3-shaped MLA decode: B={inp.B} x {ctx}, H={inp.H}, d_c=512, d_r=64, "
+                        f"page 64, n_q={inp.n_q}",
+            "batch": inp.B, "context": int(lens[0]) if (lens == lens[0]).all() else float(lens.mean()),
+            "heads": inp.H, "n_q": inp.n_q,
             "page_size": 64, "num_splits": num_splits, "cache_bytes": int(inp.seq_lens.sum()) * 1152,
             "l2": f"inputs larger than L2: {NSETS} rotating input sets of ~190 MB (latent cache, weights, "
                   "queries, tables), steps back to back, no flush"}
@@ -197,8 +201,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     mla.build()
 
-    inp = mi.workload_inputs(WORKLOAD_INDEX)
-    pg = mi.make_paged(inp, spare_pages=mi.WORKLOADS[WORKLOAD_INDEX].spare_pages)
+    inp = mi.workload_inputs(args.workload)
+    pg = mi.make_paged(inp, spare_pages=mi.WORKLOADS[args.workload].spare_pages)
     T, H, B, n_q = inp.B * inp.n_q, inp.H, inp.B, inp.n_q
 
     def to_dev(bits):
@@ -524,6 +528,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=[2, 3, 4, 5],
+                    help="the decode workload (2: 32 x 4096, the default; 3: 128 ragged; 4: 4 x 131072; "
+                         "5: 64 x 8192 with two query tokens)")
     ap.add_argument("--quick", action="store_true",
                     help="time the steps only (no phase times, end-to-end leg or CPU baseline): for profiling runs")
     ap.add_argument("--profile-phase", choices=["absorb_q_latent", "out_comb", "append_kv"], default=None,
