@@ -120,6 +120,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over the ranks of the process group (x itself without one)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, tokens_per_rank_step: int, steps: int, total_s: float) -> float:
+    """Whole-job tokens/s of replicas: every rank runs its own batch (weak scaling),
+    so all ranks' tokens over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / total_s
+
+
 def cpu_baseline(inp, budget_s: float = 12.0, max_seqs: int | None = None):
     """Time the oracle's fp32 absorbed path on whole sequences (all heads) of ``inp``."""
     import oracle
@@ -335,13 +351,9 @@ def run_ours(args):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t0_ev.elapsed_time(t1_ev)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t0_ev.elapsed_time(t1_ev), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = ws_ * T * args.steps / (total_ms * 1e-3)
+    value = job_rate(ws_, T, args.steps, total_ms * 1e-3)
 
     # per-call phase times: each call alone, R times back to back over the
     # rotating sets in one graph (the decode call is the plan and decode kernels)
@@ -422,12 +434,8 @@ def run_ours(args):
         t0 = time.perf_counter()
         e2e_step()
         e2e_times.append(time.perf_counter() - t0)
-    e2e_total = sum(e2e_times)
-    if dist is not None:
-        t = torch.tensor([e2e_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = ws_ * T * args.steps / e2e_total
+    e2e_total = max_over_ranks(sum(e2e_times), dist, dev)
+    e2e_value = job_rate(ws_, T, args.steps, e2e_total)
 
     if rank == 0:
         hbm, tflops, src = peaks()

@@ -1,0 +1,70 @@
+"""The benchmark's multi-process path (replicas, no data-path collective), on CPU.
+
+Under torchrun every rank runs its own decode batch on its own GPU; the only
+collectives are the barrier around the timed region and the max over ranks of
+the timed durations. Here two gloo ranks on 127.0.0.1 stand in for the GPUs:
+each reports its own duration, both must see the largest, and the job's rate
+counts every rank's tokens over that slowest time. Ranks other than 0 of the
+reference arm exit without work or output.
+"""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, durations, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, local = bench.dist_env()
+        assert (ws, r, local) == (world, rank, rank)
+        dist.barrier()
+        slowest = bench.max_over_ranks(durations[rank], dist, "cpu")
+        out[rank] = (slowest, bench.job_rate(ws, 32, 10, slowest))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_rate_with_two_gloo_ranks():
+    world, port = 2, _free_port()
+    durations = [0.5, 0.8]
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank_main, args=(world, port, durations, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0] == res[1]
+    slowest, rate = res[0]
+    assert slowest == 0.8
+    assert rate == pytest.approx(world * 32 * 10 / 0.8)
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(1.25, None, "cpu") == 1.25
+    assert bench.job_rate(1, 32, 100, 2.0) == 1600.0
+
+
+def test_reference_arm_other_ranks_exit_without_output():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
