@@ -45,7 +45,7 @@ def _rank_main(rank, world, port, durations, out):
 def test_max_over_ranks_and_job_rate_with_two_gloo_ranks():
     world, port = 2, _free_port()
     durations = [0.5, 0.8]
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (threaded) process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, durations, out), nprocs=world, join=True)
         res = dict(out)
