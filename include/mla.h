@@ -44,6 +44,10 @@
  *     the first nonzero mla_status into *err_word (a device int32 the caller
  *     zeroes and reads after its own synchronisation). The kernels then clamp
  *     the bad value and finish without faulting; the results are not valid.
+ *     The calls without an err_word (the projections, merges and merged-weight
+ *     products) read no index from their inputs; their only device-side
+ *     failure is a wait that gives up (about 2 s, a GPU fault), after which
+ *     the kernel finishes without faulting and leaves its output incomplete.
  */
 #ifndef MLA_GB300_H
 #define MLA_GB300_H
