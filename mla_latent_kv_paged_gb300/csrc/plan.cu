@@ -4,9 +4,10 @@
 // for the switch (the accumulator of the finished piece is written out and
 // the next query is loaded), so every sequence start after the first counts
 // as kSwitchPages extra pages: the cuts are equal steps along that longer
-// line, and a cut that falls inside a switch lands on the sequence start. Flash-decoding over a paged cache: the Huny's Dev
-// Blog "MLA 아키텍처 해부" section 4 table names FlashDecoding / PagedAttention
-// as the decode techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
+// line, and a cut that falls inside a switch lands on the sequence start.
+// Flash-decoding over a paged cache: the Huny's Dev Blog "MLA 아키텍처 해부"
+// section 4 table names FlashDecoding / PagedAttention as the decode
+// techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
 //
 // One block of 256 threads. Integer work only; the output is a pure function
 // of (seq_lens, n_q, max_pages, G), so repeated calls give identical plans.

@@ -15,9 +15,14 @@
 //   D[v][t] = sum_c W_UV[h][v][c] u[t][h][c]            M = 128 value cols, N = rows t, K = 512
 //   A = W_UV[h] (K-major), B = u rows (K-major). Each 64-wide K slice has its
 //   own barrier, so the MMAs of a slice start as soon as it lands.
-// D sits in tensor memory with one lane per output column, so the epilogue
-// writes each output row t with 32 consecutive columns per warp. N (rows per
-// tile) is 32, 64 or 128, the smallest that holds the batch's rows.
+// The absorb path also performs the value/output merge (Huny's Dev Blog
+// section 3 item 2, W_comb = W^UV W^O per head): the rows of W_O
+// [d_model][H][128] in place of query rows and W_UV (stored like W_UK) give
+// W_comb [d_model][H][512].
+// D sits in tensor memory with one lane per output column; the epilogue puts
+// the [rows][128 columns] tile through shared memory and writes each output
+// row as 16-byte stores. N (rows per tile) is 32, 64 or 128, the smallest
+// that holds the batch's rows.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
