@@ -443,7 +443,17 @@ def run_ours(args):
         dec_us = phases["decode_paged_planned"]
         dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
         achieved = dec_bytes / (dec_us * 1e-6) / 1e9
-        traffic = stored_traffic()
+        # the bound: HBM below the ridge point of the measured peaks, the tensor pipe above
+        # it (two query tokens per sequence double the flops per cached byte)
+        intensity = wb["decode_flops"] / dec_bytes
+        if intensity <= tflops * 1e12 / (hbm * 1e9):
+            bound = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
+        else:
+            tf = wb["decode_flops"] / (dec_us * 1e-6) / 1e12
+            bound = {"bound": "tensor", "achieved": tf, "peak": tflops, "unit": "TFLOP/s", "frac": tf / tflops,
+                     "hbm_gbs_achieved": achieved}
+        bound["flop_per_byte"] = intensity
+        traffic = stored_traffic(args.workload)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -451,8 +461,7 @@ def run_ours(args):
             "config": workload_config(inp, G),
             "phases_us": phases,
             "single_step_flushed_us": float(np.median(single)),
-            "roofline": {"kernel": "mla_decode_paged_planned (the split-KV decode kernel)", "bound": "hbm",
-                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "roofline": {"kernel": "mla_decode_paged_planned (the split-KV decode kernel)", **bound,
                          "traffic": traffic, "peak_source": src,
                          "alg_bytes_per_launch": dec_bytes, "alg_flops_per_launch": wb["decode_flops"],
                          "tflops_achieved": wb["decode_flops"] / (dec_us * 1e-6) / 1e12,
@@ -505,9 +514,15 @@ def comb_line(us, out_proj_us, T, H, hbm):
             "unmerged_weight_bytes": H * 128 * 512 * 2 + D_MODEL * H * 128 * 2, "out_proj_us": out_proj_us}
 
 
-def stored_traffic():
-    """dram bytes per decode launch from the committed ncu summary, if the kernel is unchanged."""
-    path = os.path.join(ROOT, "profiles", "decode_tc_v3_b32_l4096.md")
+TRAFFIC_PROFILES = {2: "decode_tc_v3_b32_l4096.md", 4: "decode_tc_long_b4_l131072.md"}
+
+
+def stored_traffic(workload: int = WORKLOAD_INDEX):
+    """dram bytes per decode launch from the committed ncu summary of this workload, if the
+    kernel is unchanged since (None otherwise)."""
+    if workload not in TRAFFIC_PROFILES:
+        return None
+    path = os.path.join(ROOT, "profiles", TRAFFIC_PROFILES[workload])
     try:
         kv = dict(ln.split(":", 1) for ln in open(path) if ln.startswith(("traffic_bytes_per_launch:", "kernel_rev:")))
         if kv.get("kernel_rev", "").strip() == mla_kernel_rev():
