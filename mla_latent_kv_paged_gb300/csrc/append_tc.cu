@@ -198,13 +198,8 @@ cudaError_t launch_gemm(const CUtensorMap& mw, const CUtensorMap& mh, int d_mode
                         const AppendShape& a, int32_t* err_word, cudaStream_t s) {
   const int max_nkb = (a.KB + a.S - 1) / a.S;
   const size_t smem = (size_t)max_nkb * (kABox + kNT * 128) + 64;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(append_gemm_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kSmemBudget + 1024));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_limit<append_gemm_kernel<kNT>>(kSmemBudget + 1024);
+  if (e != cudaSuccess) return e;
   const dim3 grid(kMTiles, a.S, a.tiles);
   return launch_pdl(append_gemm_kernel<kNT>, grid, dim3(kThreads), smem, s, mw, mh, d_model, partials, a.S,
                     err_word);

@@ -189,13 +189,8 @@ template <int kNT>
 cudaError_t launch_comb_gemm(const CUtensorMap& mw, const CUtensorMap& mu, const CombShape& c, int d_model,
                              float* partials, cudaStream_t s) {
   using C = CombCfg<kNT>;
-  static bool done = false;
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(comb_gemm_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
+  cudaError_t e = smem_limit<comb_gemm_kernel<kNT>>(C::kSmem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(comb_gemm_kernel<kNT>, dim3(c.ntiles, c.S, c.ttiles), dim3(kThreads), C::kSmem, s, mw, mu,
                     c.KB, d_model, partials);
 }

@@ -717,12 +717,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 
 // ---------------------------------------------------------------- host side
 int decode_max_workers() {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
+  if (smem_limit<decode_tc_kernel>(kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
@@ -756,13 +753,8 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
       !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64) ||
       !make_tmap(&map_q, q_abs, 2, q_dims, row_stride, box_q, 128))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_limit<decode_tc_kernel>(kSmemBytes);
+  if (e != cudaSuccess) return e;
   const float sl2 = scale * 1.4426950408889634f;
   dim3 grid(2 * G, n_q, 1);
   return launch_pdl(decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, map_q,

@@ -180,13 +180,8 @@ template <int kNT>
 cudaError_t launch_latent(const CUtensorMap& mw, const CUtensorMap& mc, const uint16_t* q_rope, uint16_t* q_abs,
                           int T, int H, int d_q, cudaStream_t s) {
   using C = LatentCfg<kNT>;
-  static bool done = false;
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(absorb_latent_kernel<kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
+  cudaError_t e = smem_limit<absorb_latent_kernel<kNT>>(C::kSmem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(absorb_latent_kernel<kNT>, dim3(H, kDC / 128), dim3(kThreads), C::kSmem, s, mw, mc, q_rope,
                     q_abs, T, H, d_q);
 }

@@ -202,13 +202,8 @@ template <bool kAbsorb, int kNT>
 cudaError_t launch_proj(const CUtensorMap& ma, const CUtensorMap& mb, const uint16_t* w, const uint16_t* q_rope,
                         uint16_t* out, int T, int H, int out_row, cudaStream_t s) {
   using C = ProjCfg<kAbsorb, kNT>;
-  static bool done = false;
-  if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel<kAbsorb, kNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
+  cudaError_t e = smem_limit<proj_tc_kernel<kAbsorb, kNT>>(C::kSmem);
+  if (e != cudaSuccess) return e;
   const dim3 grid(H, kAbsorb ? kDC / 128 : 1);
   return launch_pdl(proj_tc_kernel<kAbsorb, kNT>, grid, dim3(kThreads), C::kSmem, s, ma, mb, w, q_rope, out, T,
                     H, out_row, (int32_t*)nullptr);
