@@ -120,6 +120,21 @@ def dist_env():
     return ws, rank, local
 
 
+def roofline_bound(flops: float, nbytes: float, us: float, hbm_gbs: float, tflops: float) -> dict:
+    """The roofline a kernel sits under: HBM below the ridge point of the peaks (flops per
+    byte at which both take the same time), the tensor pipe above it."""
+    intensity = flops / nbytes
+    gbs = nbytes / (us * 1e-6) / 1e9
+    if intensity <= tflops * 1e12 / (hbm_gbs * 1e9):
+        out = {"bound": "hbm", "achieved": gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gbs / hbm_gbs}
+    else:
+        tf = flops / (us * 1e-6) / 1e12
+        out = {"bound": "tensor", "achieved": tf, "peak": tflops, "unit": "TFLOP/s", "frac": tf / tflops,
+               "hbm_gbs_achieved": gbs}
+    out["flop_per_byte"] = intensity
+    return out
+
+
 def max_over_ranks(x: float, dist, device) -> float:
     """The largest x over the ranks of the process group (x itself without one)."""
     if dist is None:
@@ -443,16 +458,7 @@ def run_ours(args):
         dec_us = phases["decode_paged_planned"]
         dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
         achieved = dec_bytes / (dec_us * 1e-6) / 1e9
-        # the bound: HBM below the ridge point of the measured peaks, the tensor pipe above
-        # it (two query tokens per sequence double the flops per cached byte)
-        intensity = wb["decode_flops"] / dec_bytes
-        if intensity <= tflops * 1e12 / (hbm * 1e9):
-            bound = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm}
-        else:
-            tf = wb["decode_flops"] / (dec_us * 1e-6) / 1e12
-            bound = {"bound": "tensor", "achieved": tf, "peak": tflops, "unit": "TFLOP/s", "frac": tf / tflops,
-                     "hbm_gbs_achieved": achieved}
-        bound["flop_per_byte"] = intensity
+        bound = roofline_bound(wb["decode_flops"], dec_bytes, dec_us, hbm, tflops)
         traffic = stored_traffic(args.workload)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_, "steps": args.steps,

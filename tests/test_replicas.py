@@ -68,3 +68,18 @@ def test_reference_arm_other_ranks_exit_without_output():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_roofline_bound_follows_the_ridge_point():
+    """Below the ridge (peak flops / peak bytes) the bound is HBM, above it the tensor pipe;
+    the fraction is the achieved rate over that peak."""
+    sys.path.insert(0, ROOT)
+    import bench
+    hbm, tf = 6775.6, 1946.8  # ridge ~287 flop/B
+    one = bench.roofline_bound(flops=234e6 * 1000, nbytes=1e9, us=200.0, hbm_gbs=hbm, tflops=tf)
+    assert one["bound"] == "hbm" and one["unit"] == "GB/s"
+    assert one["achieved"] == pytest.approx(5000.0) and one["frac"] == pytest.approx(5000.0 / hbm)
+    two = bench.roofline_bound(flops=468e9, nbytes=1e9, us=400.0, hbm_gbs=hbm, tflops=tf)
+    assert two["bound"] == "tensor" and two["unit"] == "TFLOP/s"
+    assert two["achieved"] == pytest.approx(1170.0) and two["frac"] == pytest.approx(1170.0 / tf)
+    assert two["flop_per_byte"] == pytest.approx(468.0)
