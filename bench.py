@@ -456,8 +456,7 @@ def run_ours(args):
         hbm, tflops, src = peaks()
         wb = mi.workload_bytes(inp)
         dec_us = phases["decode_paged_planned"]
-        dec_bytes = wb["cache_bytes"] + T * H * 576 * 2 + B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
-        achieved = dec_bytes / (dec_us * 1e-6) / 1e9
+        dec_bytes, _ = decode_alg(inp)
         bound = roofline_bound(wb["decode_flops"], dec_bytes, dec_us, hbm, tflops)
         traffic = stored_traffic(args.workload)
         line = {
@@ -483,11 +482,95 @@ def run_ours(args):
             "clocks": clk,
             "wall_s_timed_region": wall,
         }
+        if ws_ == 1 and not args.no_workloads:
+            line["workloads"] = side_workloads(mla, dev, err, hbm, tflops, src, exclude=args.workload)
         if ws_ == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(inp, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def decode_alg(inp):
+    """Algorithmic bytes and flops of one decode-kernel launch: the cache read once, the absorbed
+    queries, lengths and block-table entries in use (the split partials are not counted)."""
+    wb = mi.workload_bytes(inp)
+    T, H = inp.B * inp.n_q, inp.H
+    nbytes = wb["cache_bytes"] + T * H * 576 * 2 + inp.B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4
+    return nbytes, wb["decode_flops"]
+
+
+def side_workloads(mla, dev, err, hbm, tflops, src, exclude=None, calls=20, reps=10):
+    """The pages' other decode workloads (ragged batch, long contexts, two query tokens), one
+    input set each (every latent cache is 0.6-1.25 GB, far beyond L2): the decode kernel's time
+    per call and its roofline, and the whole step's, each as ``calls`` back-to-back calls in a
+    CUDA graph replayed ``reps`` times (median)."""
+    import torch
+    res = {}
+    stream = torch.cuda.current_stream()
+    names = {3: "ragged", 4: "long_context", 5: "two_query_tokens"}
+    for idx in (3, 4, 5):
+        if idx == exclude:
+            continue
+        inp = mi.workload_inputs(idx)
+        pg = mi.make_paged(inp, spare_pages=mi.WORKLOADS[idx].spare_pages)
+        T, H, B, n_q = inp.B * inp.n_q, inp.H, inp.B, inp.n_q
+
+        def to_dev(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        S = dict(q_nope=to_dev(inp.q_nope.reshape(T, H, -1)), q_rope=to_dev(inp.q_rope.reshape(T, H, -1)),
+                 w_uk=to_dev(inp.w_uk), w_uv=to_dev(inp.w_uv), cache=to_dev(pg.cache),
+                 bt=torch.from_numpy(pg.block_table).to(dev), sl=torch.from_numpy(inp.seq_lens).to(dev))
+        G = mla.default_splits(n_q)
+        bufs = dict(q_abs=torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev),
+                    workspace=torch.empty(mla.workspace_bytes(B, n_q, H, G), dtype=torch.uint8, device=dev),
+                    u=torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev),
+                    lse=torch.empty((T, H), dtype=torch.float32, device=dev),
+                    out=torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev))
+
+        def step():
+            mla.decode_step(S["q_nope"], S["q_rope"], S["w_uk"], S["w_uv"], S["cache"], S["bt"], S["sl"], n_q=n_q,
+                            num_splits=G, bufs=bufs, err_word=err)
+
+        def decode_planned():
+            mla.decode_paged(bufs["q_abs"], S["cache"], S["bt"], S["sl"], n_q=n_q, num_splits=G,
+                             workspace=bufs["workspace"], err_word=err, planned=True)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise SystemExit(f"device error word {int(err.item())} on workload {idx}")
+
+        def timed(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(calls):
+                    fn()
+            g.replay()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return 1e3 * float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])) / calls
+
+        step_us = timed(step)
+        dec_us = timed(decode_planned)  # the plan of the last step is in the workspace
+        nbytes, flops = decode_alg(inp)
+        bound = roofline_bound(flops, nbytes, dec_us, hbm, tflops)
+        res[names[idx]] = {
+            "workload": workload_config(inp, G)["workload"], "decode_us": dec_us, "step_us": step_us,
+            "tokens_per_s": T / (step_us * 1e-6), "alg_bytes_per_launch": nbytes, "alg_flops_per_launch": flops,
+            **bound, "tflops_achieved": flops / (dec_us * 1e-6) / 1e12, "peak_source": src,
+            "traffic": stored_traffic(idx),
+            "duration": f"per call, {calls} calls back to back in a CUDA graph, median of {reps} replays"}
+        del S, bufs
+        torch.cuda.empty_cache()
+    return res
 
 
 def append_line(us, T, hbm):
@@ -557,6 +640,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the 'workloads' block (the ragged, long-context and two-token decode workloads)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX, choices=[2, 3, 4, 5],
                     help="the decode workload (2: 32 x 4096, the default; 3: 128 ragged; 4: 4 x 131072; "
                          "5: 64 x 8192 with two query tokens)")

@@ -287,8 +287,12 @@ mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_spl
  *
  * The first call made with a device current looks up the array's device
  * address (cudaGetSymbolAddress); make that first call before any stream
- * capture. All calls share the array: calls whose kernels overlap on the
- * GPU (other streams, other host threads) race on it. Arguments and results
+ * capture. The address is kept with the unique id of the context it belongs
+ * to; the first call under another context (for example after
+ * cudaDeviceReset, which recreates the device's primary context) looks it up
+ * again and must also come before any stream capture. All calls share the
+ * array: calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on it. Arguments and results
  * are those of mla_decode_paged and mla_combine (u [B][n_q][H][512] bf16,
  * lse [B][n_q][H] float or NULL). Nothing is allocated or freed. */
 size_t mla_decode_noalloc_max_bytes(void);

@@ -79,11 +79,19 @@ WORKLOADS = {
 # bf16 helpers (bit patterns held in uint16 arrays)
 # ----------------------------------------------------------------------------
 def f32_to_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even); NaN -> 0x7FC0."""
+    """Round float32 values to bf16 (nearest, ties to even); NaN -> 0x7FC0.
+
+    In 32-bit arithmetic: for every finite or infinite input the sum below stays
+    under 2^32 (the largest bit pattern, -inf, is 0xFF800000); only NaN patterns
+    can wrap, and those are replaced afterwards."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rnd = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
-    out = ((u + rnd) >> np.uint64(16)).astype(np.uint16)
+    u = x.view(np.uint32)
+    t = u >> np.uint32(16)
+    t &= np.uint32(1)
+    t += np.uint32(0x7FFF)
+    t += u
+    t >>= np.uint32(16)
+    out = t.astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         out[nan] = BF16_NAN
@@ -178,6 +186,29 @@ def make_inputs(B: int, H: int, n_q: int, seq_lens, seed: int, *,
         w_uk=f32_to_bf16(w_uk), w_uv=f32_to_bf16(w_uv),
         meta={"seed": seed},
     )
+
+
+def with_rising_scores(inp: Inputs, *, gamma: float = 8.0, top: float = 64.0, col: int = 0,
+                       kind: str = "ramp") -> Inputs:
+    """A copy of ``inp`` whose later tokens score higher for every head, by a shift that
+    bf16 holds exactly: column ``col`` of every (rotated) positional query is set to
+    ``gamma`` and column ``col`` of token s's positional key to beta(s / L), with
+    beta(x) = top * x ("ramp") or top * [x >= 1/2] ("step"), rounded to bf16. Every
+    head's score of token s then grows by gamma * beta(s / L) / sqrt(192) (37 in
+    natural-log units for the defaults), so the running softmax maximum keeps rising
+    along a sequence. The rest of the inputs are those of ``inp``."""
+    import dataclasses
+    qr = bf16_to_f32(inp.q_rope).copy()
+    qr[..., col] = gamma
+    kr = bf16_to_f32(inp.kr).copy()
+    for b in range(inp.B):
+        L = int(inp.seq_lens[b])
+        o = int(inp.seq_off[b])
+        x = np.arange(L, dtype=np.float64) / L
+        beta = top * x if kind == "ramp" else top * (x >= 0.5)
+        kr[o:o + L, col] = beta.astype(np.float32)
+    return dataclasses.replace(inp, q_rope=f32_to_bf16(qr), kr=f32_to_bf16(kr),
+                               meta=dict(inp.meta, rising=(gamma, top, col, kind)))
 
 
 def workload_inputs(index: int) -> Inputs:

@@ -55,13 +55,18 @@ class MlaError(RuntimeError):
         super().__init__(f"{where}: {STATUS.get(status, status)}")
 
 
+DEBUG_LIB_PATH = os.path.join(_HERE, "libmla_gb300_debug.so")
+DEBUG_EXPORTS = ["mla_debug_read_counters", "mla_debug_reset", "mla_debug_set_wait_limit",
+                 "mla_debug_set_skip_producer"]
+
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
 
 
-def build(force: bool = False) -> str:
+def build(force: bool = False, debug: bool = False) -> str:
     from . import _build
-    return _build.build(force=force)
+    return _build.build(force=force, debug=debug)
 
 
 def lib():
@@ -69,52 +74,75 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise ImportError(f"{LIB_PATH} is missing; run __graft_entry__.build() first")
-            L = ctypes.CDLL(LIB_PATH)
-            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-            L.mla_status_string.restype = ctypes.c_char_p
-            L.mla_status_string.argtypes = [i]
-            L.mla_abi_version.restype = i
-            L.mla_cache_bytes_per_token.restype = sz
-            L.mla_cache_bytes_per_token.argtypes = [i, i]
-            L.mla_page_bytes.restype = sz
-            L.mla_page_bytes.argtypes = [i, i, i]
-            L.mla_absorb_q.restype = i
-            L.mla_absorb_q.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
-            L.mla_decode_default_splits.restype = i
-            L.mla_decode_default_splits.argtypes = [i]
-            L.mla_decode_workspace_bytes.restype = sz
-            L.mla_decode_workspace_bytes.argtypes = [i, i, i, i]
-            L.mla_decode_paged.restype = i
-            L.mla_decode_paged.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
-            L.mla_decode_plan.restype = i
-            L.mla_decode_plan.argtypes = [vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
-            L.mla_decode_paged_planned.restype = i
-            L.mla_decode_paged_planned.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
-            L.mla_combine.restype = i
-            L.mla_combine.argtypes = [vp, i, i, i, i, vp, vp, vp]
-            L.mla_out_proj.restype = i
-            L.mla_out_proj.argtypes = [vp, vp, vp, i, i, i, i, vp]
-            L.mla_decode_noalloc_max_bytes.restype = sz
-            L.mla_decode_noalloc.restype = i
-            L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
-            L.mla_append_workspace_bytes.restype = sz
-            L.mla_append_workspace_bytes.argtypes = [i, i]
-            L.mla_append_kv.restype = i
-            L.mla_append_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp]
-            L.mla_merge_w_kq.restype = i
-            L.mla_merge_w_kq.argtypes = [vp, vp, vp, i, i, i, i, vp]
-            L.mla_absorb_q_latent.restype = i
-            L.mla_absorb_q_latent.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
-            L.mla_merge_w_comb.restype = i
-            L.mla_merge_w_comb.argtypes = [vp, vp, vp, i, i, i, i, vp]
-            L.mla_out_comb_workspace_bytes.restype = sz
-            L.mla_out_comb_workspace_bytes.argtypes = [i, i, i]
-            L.mla_out_comb.restype = i
-            L.mla_out_comb.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
-            _lib = L
+            _lib = _load(LIB_PATH)
     return _lib
+
+
+def debug_lib():
+    """The test build of the library (include/mla_debug.h), built on first use: the same
+    entry points plus the decode kernel's instrumentation. For tests only."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            build(debug=True)
+            L = _load(DEBUG_LIB_PATH)
+            L.mla_debug_read_counters.restype = ctypes.c_int
+            L.mla_debug_read_counters.argtypes = [ctypes.c_void_p, ctypes.c_int]
+            L.mla_debug_reset.restype = ctypes.c_int
+            L.mla_debug_set_wait_limit.restype = ctypes.c_int
+            L.mla_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+            L.mla_debug_set_skip_producer.restype = ctypes.c_int
+            L.mla_debug_set_skip_producer.argtypes = [ctypes.c_int]
+            _debug_lib = L
+    return _debug_lib
+
+
+def _load(path: str):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing; run __graft_entry__.build() first")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.mla_status_string.restype = ctypes.c_char_p
+    L.mla_status_string.argtypes = [i]
+    L.mla_abi_version.restype = i
+    L.mla_cache_bytes_per_token.restype = sz
+    L.mla_cache_bytes_per_token.argtypes = [i, i]
+    L.mla_page_bytes.restype = sz
+    L.mla_page_bytes.argtypes = [i, i, i]
+    L.mla_absorb_q.restype = i
+    L.mla_absorb_q.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    L.mla_decode_default_splits.restype = i
+    L.mla_decode_default_splits.argtypes = [i]
+    L.mla_decode_workspace_bytes.restype = sz
+    L.mla_decode_workspace_bytes.argtypes = [i, i, i, i]
+    L.mla_decode_paged.restype = i
+    L.mla_decode_paged.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
+    L.mla_decode_plan.restype = i
+    L.mla_decode_plan.argtypes = [vp, i, i, i, i, i, i, i, vp, sz, vp, vp]
+    L.mla_decode_paged_planned.restype = i
+    L.mla_decode_paged_planned.argtypes = [vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
+    L.mla_combine.restype = i
+    L.mla_combine.argtypes = [vp, i, i, i, i, vp, vp, vp]
+    L.mla_out_proj.restype = i
+    L.mla_out_proj.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.mla_decode_noalloc_max_bytes.restype = sz
+    L.mla_decode_noalloc.restype = i
+    L.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    L.mla_append_workspace_bytes.restype = sz
+    L.mla_append_workspace_bytes.argtypes = [i, i]
+    L.mla_append_kv.restype = i
+    L.mla_append_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz, vp, vp]
+    L.mla_merge_w_kq.restype = i
+    L.mla_merge_w_kq.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.mla_absorb_q_latent.restype = i
+    L.mla_absorb_q_latent.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    L.mla_merge_w_comb.restype = i
+    L.mla_merge_w_comb.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.mla_out_comb_workspace_bytes.restype = sz
+    L.mla_out_comb_workspace_bytes.argtypes = [i, i, i]
+    L.mla_out_comb.restype = i
+    L.mla_out_comb.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
+    return L
 
 
 def _ptr(t):
@@ -305,24 +333,22 @@ def combine(workspace, *, B: int, n_q: int, H: int, num_splits: int, u=None, lse
     return u, lse
 
 
-def decode_noalloc(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
-                   softmax_scale: float = DEFAULT_SCALE, u=None, lse=None, err_word=None, stream=None):
+def decode_noalloc(q_abs, cache, block_table, seq_lens, *, n_q: int, u, lse=None, num_splits: int | None = None,
+                   softmax_scale: float = DEFAULT_SCALE, err_word=None, stream=None):
     """decode_paged + combine with the scratch kept inside the library (no workspace).
 
-    For callers that must not allocate device memory during a step; see
-    ``mla_decode_noalloc`` in include/mla.h for the size limit and for the
-    rule that calls overlapping on the GPU race on the shared scratch.
+    For callers that must not allocate device memory during a step: neither this
+    wrapper nor the C call allocates, so the outputs come from the caller, u
+    [B*n_q, H, 512] bf16 and (optional, None skips it) lse [B*n_q, H] float32. See
+    ``mla_decode_noalloc`` in include/mla.h for the size limit and for the rule
+    that calls overlapping on the GPU race on the shared scratch.
     """
-    import torch
     B, max_pages = block_table.shape
     H = q_abs.shape[-2]
     if num_splits is None:
         num_splits = default_splits(n_q)
-    dev = q_abs.device
     if u is None:
-        u = torch.empty((B * n_q, H, D_C), dtype=torch.bfloat16, device=dev)
-    if lse is None:
-        lse = torch.empty((B * n_q, H), dtype=torch.float32, device=dev)
+        raise ValueError("decode_noalloc: pass the output tensor u (this call allocates nothing)")
     st = lib().mla_decode_noalloc(_ptr(_bits(q_abs)), _ptr(_bits(cache)), _ptr(block_table), _ptr(seq_lens),
                                   B, n_q, H, cache.shape[0], cache.shape[1], max_pages, float(softmax_scale),
                                   num_splits, _ptr(_bits(u)), _ptr(lse), _ptr(err_word), _stream(stream))

@@ -63,11 +63,14 @@ constexpr uint32_t kStageBytes = 4 * kCBoxBytes + kKrBoxBytes;  // 36864
 constexpr uint32_t kQrBoxBytes = 64 * 64;   // [64 heads][32 positional cols] bf16, 64B swizzle
 constexpr uint32_t kQBoxBytes = 128 * 128;  // [128 heads][64 latent cols] bf16, 128B swizzle
 constexpr int kQSlots = 2;                  // ring slots taken by a range's latent query half (4 boxes)
-constexpr uint32_t kXBytes = 4 * 128 * 16;  // peer partial scores: [4 groups of 8 tokens][128 heads] fp16  // + the peer's partial-score maximum per head (fp32)
+constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
+// peer partial scores: [4 groups of 8 tokens][128 heads] fp16 offsets from a per-head
+// midpoint, then the midpoints [128 heads] fp32 (log2 units)
+constexpr uint32_t kXDataBytes = 4 * 128 * 16;
+constexpr uint32_t kXBytes = kXDataBytes + kVecBytes;
 constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads][32 tokens] bf16, 64B swizzle
 constexpr uint32_t kPHalfBytes = kPPeerBytes;
 constexpr int kPBufs = 3;  // P buffers: page g uses g % 3, so its writers wait for page g - 3
-constexpr uint32_t kVecBytes = 128 * 4;     // one float per head
 constexpr uint32_t kTokBytes = 4 * 4;       // "partial consumed" tokens: one per warp of a group
 
 constexpr uint32_t kOffStage = 0;
@@ -102,6 +105,31 @@ static_assert(2 * kQBoxBytes + kQrBoxBytes <= kStageBytes, "a ring slot holds a 
 constexpr uint32_t kTmO = 0, kTmS = 256, kTmP = 320, kTmQr = 368, kTmQ = 384, kTmCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay <= 256
+
+#if MLA_DEBUG_CHECKS
+// Test builds only (libmla_gb300_debug.so): counters read by the host through
+// mla_debug_read_counters, and a switch that keeps the producer from loading
+// anything so that the consumers' bounded waits give up.
+//   [0] warps that rescaled O (the running maximum rose past the threshold)
+//   [1] shared-memory or tensor-memory addresses outside this CTA's allocation
+__device__ unsigned long long g_dbg_counters[4];
+__device__ int g_dbg_skip_producer;
+__device__ __noinline__ bool dbg_check(bool ok, int32_t* err_word) {
+  if (!ok) {
+    atomicAdd(&g_dbg_counters[1], 1ull);
+    report_error(err_word, MLA_ERR_BOUNDS);
+  }
+  return ok;
+}
+// true when [addr, addr + bytes) lies inside this CTA's dynamic shared memory
+// (for an address of the peer CTA: the same offset before mapa)
+#define MLA_SMEM_OK(addr, bytes) \
+  dbg_check((addr) >= sbase && (uint64_t)(addr) + (bytes) <= (uint64_t)sbase + kSmemBytes, err_word)
+#define MLA_TMEM_OK(col, ncols) dbg_check((uint32_t)(col) + (ncols) <= (uint32_t)kTmCols, err_word)
+#else
+#define MLA_SMEM_OK(addr, bytes) true
+#define MLA_TMEM_OK(col, ncols) true
+#endif
 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -219,6 +247,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     };
     Cursor ld;
     cur_init(ld, it0);
+#if MLA_DEBUG_CHECKS
+    if (*reinterpret_cast<volatile int*>(&g_dbg_skip_producer)) ld.it = it1;  // load nothing
+#endif
     while (ok && ld.it < it1) {
       const int it = ld.it;
       if (ld.pg == plan.item_page0[it]) {
@@ -229,7 +260,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         const int qrow = (plan.item_seq[it] * n_q + j) * H;
         for (int q = 0; q < kQSlots && ok; ++q) {
           if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
-          if (lane == 0) {
+          if (lane == 0 && MLA_SMEM_OK(sbase + kOffStage + stage * kStageBytes, kStageBytes)) {
             const uint32_t fb = bar(FULL0 + stage);
             const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
             mbar_arrive_expect_tx(fb, 2 * kQBoxBytes + kQrBoxBytes);
@@ -247,7 +278,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       // an id outside the pool loads zeros (TMA bounds) and is reported
       if (lane == 0 && (pid < 0 || pid >= num_pages)) report_error(err_word, MLA_ERR_BOUNDS);
       if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
-      if (lane == 0) {
+      if (lane == 0 && MLA_SMEM_OK(sbase + kOffStage + stage * kStageBytes, kStageBytes)) {
         const uint32_t fb = bar(FULL0 + stage);
         const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
         mbar_arrive_expect_tx(fb, kStageBytes);
@@ -387,7 +418,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       bool ok = true;
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
-        const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+        const int pg0 = plan.item_page0[it];
+        const int ntiles = plan.item_page1[it] - pg0;
+        const int n_att = plan.seq_len_eff[plan.item_seq[it]] - n_q + j + 1;  // tokens query j attends
         // the range's latent query half: this thread's head row from the two ring
         // slots (four [128][64] boxes, 128B-swizzled: 16-byte chunk c of row r at
         // c ^ (r % 8)) into tensor memory. The previous range's score MMAs are done
@@ -396,6 +429,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           const int slot = g + kQSlots * li + q;
           if (!wait_phase(bar(FULL0 + slot % kStages), (slot / kStages) & 1, abort_flag, err_word)) { ok = false; break; }
           const uint32_t sq = sbase + kOffStage + (slot % kStages) * kStageBytes + (uint32_t)row * 128;
+          (void)MLA_SMEM_OK(sq + kQBoxBytes, 128);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             uint32_t r[32];
@@ -435,16 +469,46 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             if (!wait_phase(bar(XE0 + (g & 1)), ((g >> 1) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
             if (atid == 0) mbar_arrive_expect_tx(bar(XE0 + (g & 1)), kTokBytes);  // arm for this page
           }
-          const uint32_t xa = r_x + (uint32_t)(g & 1) * kXBytes + (uint32_t)row * 16;
-          const uint32_t xf = r_xf + 8u * (uint32_t)(g & 1);
+          // The partial scores go out as fp16 offsets from the midpoint of this head's
+          // values (sent in fp32): the rounding error then follows the spread of the
+          // scores within the 32 tokens, not their size (a score shared by the tokens
+          // costs no precision). Only tokens the query attends count toward the
+          // midpoint; slack rows past the context may hold any bits.
+          float v[32];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 w;
-            w.x = cvt_f16x2(__uint_as_float(r[8 * q8 + 0]) * sl2, __uint_as_float(r[8 * q8 + 1]) * sl2);
-            w.y = cvt_f16x2(__uint_as_float(r[8 * q8 + 2]) * sl2, __uint_as_float(r[8 * q8 + 3]) * sl2);
-            w.z = cvt_f16x2(__uint_as_float(r[8 * q8 + 4]) * sl2, __uint_as_float(r[8 * q8 + 5]) * sl2);
-            w.w = cvt_f16x2(__uint_as_float(r[8 * q8 + 6]) * sl2, __uint_as_float(r[8 * q8 + 7]) * sl2);
-            st_async_v4(xa + q8 * 128 * 16, w, xf);
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * sl2;
+          const int nvp = n_att - ((pg0 + i) * kPage + 32 * (int)peer);  // attended among the 32
+          float hi = -INFINITY, lo = INFINITY;
+          if (nvp >= 32) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              hi = fmaxf(hi, v[k]);
+              lo = fminf(lo, v[k]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (k < nvp) {
+                hi = fmaxf(hi, v[k]);
+                lo = fminf(lo, v[k]);
+              }
+          }
+          const float mid = lo <= hi ? 0.5f * lo + 0.5f * hi : 0.f;
+          const uint32_t xoff = (uint32_t)(g & 1) * kXBytes;
+          const uint32_t xa = r_x + xoff + (uint32_t)row * 16;
+          const uint32_t xf = r_xf + 8u * (uint32_t)(g & 1);
+          if (MLA_SMEM_OK(sbase + kOffX + xoff + (uint32_t)row * 16 + 3 * 128 * 16, 16) &&
+              MLA_SMEM_OK(sbase + kOffX + xoff + kXDataBytes + (uint32_t)row * 4, 4)) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              uint4 w;
+              w.x = cvt_f16x2(v[8 * q8 + 0] - mid, v[8 * q8 + 1] - mid);
+              w.y = cvt_f16x2(v[8 * q8 + 2] - mid, v[8 * q8 + 3] - mid);
+              w.z = cvt_f16x2(v[8 * q8 + 4] - mid, v[8 * q8 + 5] - mid);
+              w.w = cvt_f16x2(v[8 * q8 + 6] - mid, v[8 * q8 + 7] - mid);
+              st_async_v4(xa + q8 * 128 * 16, w, xf);
+            }
+            st_async_b32(r_x + xoff + kXDataBytes + (uint32_t)row * 4, __float_as_uint(mid), xf);
           }
         }
       }
@@ -528,13 +592,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             tmem_ld32(tS + 32 * rank, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int v = 0; v < 32; ++v) x[v] = __uint_as_float(r[v]) * sl2;
+            for (int v = 0; v < 32; ++v) x[v] = __uint_as_float(r[v]);  // scaled below
           }
           tc_fence_before();
           mbar_arrive(bar(SFREE));
-          // add the peer's partial for these tokens
+          // add the peer's partial for these tokens: its midpoint plus the fp16 offsets
           if (!wait_phase(bar(XF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           if (gtid == 0) mbar_arrive_expect_tx(bar(XF0 + xb), kXBytes);  // arm for page g+2
+          float mid_p;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(mid_p) : "r"(sbase + kOffX + xb * kXBytes + kXDataBytes + vec_off));
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
             uint4 w;
@@ -545,8 +611,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const float2 f = f16x2_to_f32(ww[k]);
-              x[8 * q8 + 2 * k] += f.x;
-              x[8 * q8 + 2 * k + 1] += f.y;
+              x[8 * q8 + 2 * k] = fmaf(x[8 * q8 + 2 * k], sl2, mid_p) + f.x;
+              x[8 * q8 + 2 * k + 1] = fmaf(x[8 * q8 + 2 * k + 1], sl2, mid_p) + f.y;
             }
           }
           __syncwarp();
@@ -570,6 +636,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             // stage (SF); the value MMAs read it after this group's P-ready arrive.
             const int stage = (g + kQSlots * (li + 1)) % kStages;  // ring slot of page g
             const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
+            (void)MLA_SMEM_OK(sa, 4 * kCBoxBytes);
             const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
             for (int z = gtid; z < nz; z += kGThreads) {
               const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
@@ -606,6 +673,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kOffMR + vec_off), "f"(m_new) : "memory");
           mbar_arrive(bar(MRF));
           if (__any_sync(0xffffffffu, need)) {
+#if MLA_DEBUG_CHECKS
+            if (lane == 0) atomicAdd(&g_dbg_counters[0], 1ull);
+#endif
             // O must hold every earlier page before it is rescaled
             if (!wait_phase(bar(PVD0 + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
@@ -633,6 +703,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           // shared memory (64B-swizzled, K-major) for its own
           const uint32_t pr = r_p + pb * kPPeerBytes + (uint32_t)row * 64;
           const uint32_t pfr = r_pf + 8u * pb;
+          (void)MLA_SMEM_OK(sbase + kOffP + pb * kPPeerBytes + (uint32_t)row * 64, 64);
+          (void)MLA_TMEM_OK(kTmP + 16 * pb, 16);
           float lsum0 = 0.f, lsum1 = 0.f;
           uint32_t pw[16];
 #pragma unroll
@@ -762,3 +834,30 @@ cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const in
 }
 
 }  // namespace mla
+
+#if MLA_DEBUG_CHECKS
+// Test-build entry points (declared in include/mla_debug.h). Synchronous
+// copies to or from the decode kernel's instrumentation variables on the
+// current device; each returns a cudaError_t value (0 = success).
+extern "C" {
+int mla_debug_read_counters(unsigned long long* out, int n) {
+  if (!out || n < 1 || n > 4) return (int)cudaErrorInvalidValue;
+  return (int)cudaMemcpyFromSymbol(out, mla::g_dbg_counters, sizeof(unsigned long long) * (size_t)n);
+}
+int mla_debug_reset(void) {
+  const unsigned long long zero[4] = {0, 0, 0, 0};
+  const int off = 0;
+  const long long nolimit = 0;
+  cudaError_t e = cudaMemcpyToSymbol(mla::g_dbg_counters, zero, sizeof(zero));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(mla::g_dbg_skip_producer, &off, sizeof(off));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(mla::sm100::g_wait_limit_override, &nolimit, sizeof(nolimit));
+  return (int)e;
+}
+int mla_debug_set_wait_limit(long long cycles) {
+  return (int)cudaMemcpyToSymbol(mla::sm100::g_wait_limit_override, &cycles, sizeof(cycles));
+}
+int mla_debug_set_skip_producer(int on) {
+  return (int)cudaMemcpyToSymbol(mla::g_dbg_skip_producer, &on, sizeof(on));
+}
+}  // extern "C"
+#endif

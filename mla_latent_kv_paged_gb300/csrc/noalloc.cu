@@ -12,11 +12,17 @@
 // The array's address is fetched once per device with cudaGetSymbolAddress
 // (in host code the symbol names a host-side stand-in, not device memory).
 // That happens on the first call made with each device current, so the
-// first call on a device should come before any stream capture. All calls
-// share the one array: two calls whose kernels overlap on the GPU (different
-// streams, or different host threads) race on it and give wrong results.
-// Nothing in the array needs to start at zero: the plan kernel writes every
-// entry the later kernels read.
+// first call on a device should come before any stream capture. The address
+// belongs to the device's context: it is kept together with the context's
+// unique id, and a call made under another context (for example after
+// cudaDeviceReset, which replaces the primary context and reloads the
+// library's device code elsewhere) fetches it again, which again must happen
+// outside stream capture. All calls share the one array: two calls whose
+// kernels overlap on the GPU (different streams, or different host threads)
+// race on it and give wrong results. Nothing in the array needs to start at
+// zero: the plan kernel writes every entry the later kernels read.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "mla_internal.cuh"
@@ -30,22 +36,59 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to (never reused)
+  void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array for the current device (set-up on first use).
+// Unique id of the current context, through driver entry points fetched by the
+// runtime (no link-time dependency on the driver library).
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx) return cudaErrorContextIsDestroyed;  // none current on this thread yet
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array in the current device's context
+// (looked up on the first call under each context).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  unsigned long long id = 0;
+  e = current_context_id(&id);
+  const bool no_context = e == cudaErrorContextIsDestroyed;
+  if (e != cudaSuccess && !no_context) return e;
+  if (no_context || !g_scratch[dev].ptr || g_scratch[dev].ctx_id != id) {
+    // the lookup also makes the device's primary context current if none is
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    if (no_context) {
+      e = current_context_id(&id);
+      if (e != cudaSuccess) return e;
+    }
+    g_scratch[dev] = ScratchEntry{id, p};
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return cudaSuccess;
 }
 

@@ -95,14 +95,27 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // up, later waits return false at once.
 constexpr long long kWaitLimitCycles = 4000000000LL;  // about 2 s at 2 GHz
 
+#if MLA_DEBUG_CHECKS
+// Test builds only: a shorter limit set from the host (one copy per
+// translation unit; 0 keeps the default), so a test can make a wait give up.
+static __device__ long long g_wait_limit_override;
+__device__ __forceinline__ long long wait_limit() {
+  const long long v = *reinterpret_cast<volatile long long*>(&g_wait_limit_override);
+  return v > 0 ? v : kWaitLimitCycles;
+}
+#else
+__device__ __forceinline__ constexpr long long wait_limit() { return kWaitLimitCycles; }
+#endif
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort,
                                            int32_t* err_word, bool cluster_scope = false) {
   if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
+  const long long limit = wait_limit();
   while (true) {
     if (*abort) return false;
     if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       if (err_word) atomicCAS(err_word, 0, 5 /* MLA_ERR_TIMEOUT */);
       return false;

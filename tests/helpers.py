@@ -97,3 +97,34 @@ def plan_mirror(seq_lens, n_q, max_pages, G, page=64, switch_pages=3):
             range_item.append(glob_start.index(cut_at[p]))
     return dict(items=np.array(items, dtype=np.int64), seq_item=np.array(seq_item),
                 range_item=np.array(range_item), total=P, Ge=Ge, lens=lens, switch=a)
+
+
+def abi_step(L, d, inp, pg, num_splits=None, err=None, scale=None):
+    """One decode step through the C ABI of the ctypes library ``L`` (the release or the
+    test build): mla_absorb_q -> mla_decode_paged -> mla_combine -> mla_out_proj on the
+    device tensors ``d`` (from device_inputs). Returns dict(q_abs, u, lse, out, workspace)."""
+    import ctypes
+    import math
+
+    import torch
+    T, H = inp.B * inp.n_q, inp.H
+    dev = d["cache"].device
+    G = int(L.mla_decode_default_splits(inp.n_q)) if num_splits is None else num_splits
+    scale = 1.0 / math.sqrt(192.0) if scale is None else scale
+    q_abs = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(int(L.mla_decode_workspace_bytes(inp.B, inp.n_q, H, G)), dtype=torch.uint8, device=dev)
+    u = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device=dev)
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = L.mla_absorb_q(p(d["q_nope"]), p(d["q_rope"]), p(d["w_uk"]), p(q_abs), T, H, 128, 64, 512, s)
+    assert st == 0, ("mla_absorb_q", st)
+    st = L.mla_decode_paged(p(q_abs), p(d["cache"]), p(d["block_table"]), p(d["seq_lens"]), inp.B, inp.n_q, H,
+                            pg.num_pages, 64, pg.max_pages, ctypes.c_float(scale), G, p(ws), ws.numel(), p(err), s)
+    assert st == 0, ("mla_decode_paged", st)
+    st = L.mla_combine(p(ws), inp.B, inp.n_q, H, G, p(u), p(lse), s)
+    assert st == 0, ("mla_combine", st)
+    st = L.mla_out_proj(p(u), p(d["w_uv"]), p(out), T, H, 512, 128, s)
+    assert st == 0, ("mla_out_proj", st)
+    return dict(q_abs=q_abs, u=u, lse=lse, out=out, workspace=ws)

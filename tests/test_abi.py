@@ -19,10 +19,13 @@ def lib():
     return mla.lib()
 
 
-def declared_functions():
+DEBUG_HEADER = "mla_debug.h"  # the test build's extra entry points
+
+
+def declared_functions(headers=None):
     names = []
     for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
-        if h.endswith(".h"):
+        if h.endswith(".h") and (headers is None or h in headers):
             src = open(os.path.join(ROOT, "include", h)).read()
             src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
             names += re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)
@@ -30,12 +33,26 @@ def declared_functions():
 
 
 def test_exports_every_declared_symbol(lib):
-    decl = declared_functions()
+    release = [h for h in os.listdir(os.path.join(ROOT, "include")) if h.endswith(".h") and h != DEBUG_HEADER]
+    decl = declared_functions(release)
     assert "mla_decode_paged" in decl and "mla_combine" in decl
     for name in decl:
         assert hasattr(lib, name), name
     assert set(mla.EXPORTS) <= set(decl)
     assert lib.mla_abi_version() == 3
+    # the release library carries none of the test build's instrumentation
+    for name in declared_functions([DEBUG_HEADER]):
+        assert not hasattr(lib, name), name
+
+
+def test_test_build_exports_everything():
+    """libmla_gb300_debug.so: every declared entry point, the test-only ones included."""
+    dbg = mla.debug_lib()
+    decl = declared_functions()
+    assert set(mla.DEBUG_EXPORTS) == set(declared_functions([DEBUG_HEADER]))
+    for name in decl:
+        assert hasattr(dbg, name), name
+    assert dbg.mla_abi_version() == 3
 
 
 def test_status_strings(lib):

@@ -2,10 +2,10 @@
 
 mla_decode_noalloc serves callers that cannot hand the library a workspace:
 it keeps the split plan and partial results in a fixed array inside the
-library. Called twice in a row through the C ABI, it must give the same u and
-lse as mla_decode_paged + mla_combine with a caller-provided workspace, within
-the tolerances of the other parity tests; a request too large for the array
-must be refused before any launch.
+library. Called twice in a row through the C ABI, it must give u and lse that
+match the CPU oracle within the tolerances of the other parity tests, and the
+same values as mla_decode_paged + mla_combine with a caller-provided workspace;
+a request too large for the array must be refused before any launch.
 """
 import ctypes
 
@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 import mla_inputs as mi
+import oracle
 from tests.helpers import MAX_ABS, MEAN_REL, assert_close, dev_bf16_to_f64, dev_to_bits, device_inputs
 
 pytestmark = pytest.mark.gpu
@@ -47,6 +48,10 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert st == 0, mla.STATUS.get(st, st)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
+        ref = oracle.absorbed_f64(inp)
+        T, H = inp.B * inp.n_q, inp.H
+        assert_close(dev_bf16_to_f64(u).reshape(T * H, 512), ref["u"], "u vs oracle", MAX_ABS, MEAN_REL)
+        assert_close(lse.double().cpu().numpy().reshape(T * H), ref["lse"], "lse vs oracle", MAX_ABS, MEAN_REL)
         assert_close(dev_bf16_to_f64(u), dev_bf16_to_f64(u_ref), "u", MAX_ABS, MEAN_REL)
         assert_close(lse.double().cpu().numpy(), lse_ref.double().cpu().numpy(), "lse", MAX_ABS, MEAN_REL)
 
@@ -87,8 +92,10 @@ def test_noalloc_back_to_back_calls_with_different_lengths():
     outs = []
     for rep in range(4):  # the two calls back to back, several times
         for i, d in enumerate(ds):
+            u = torch.empty((8, H, 512), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((8, H), dtype=torch.float32, device="cuda")
             outs.append((i, mla.decode_noalloc(q_abs[i], d["cache"], d["block_table"], d["seq_lens"], n_q=1,
-                                               num_splits=20)))
+                                               u=u, lse=lse, num_splits=20)))
     torch.cuda.synchronize()
     for i, (u, lse) in outs:
         assert np.array_equal(dev_to_bits(u), dev_to_bits(refs[i][0]))
