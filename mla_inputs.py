@@ -267,6 +267,82 @@ def make_paged(inp: Inputs, *, perm_seed: int = 12345, spare_pages: int = 4,
     return Paged(cache=cache, block_table=bt, num_pages=num_pages, max_pages=max_pages, page_size=page)
 
 
+# ----------------------------------------------------------------------------
+# FP8 (e4m3) latent cache with per-channel scales
+# ----------------------------------------------------------------------------
+E4M3_MAX = 448.0  # largest finite e4m3 value: 2^8 * 1.75
+
+
+def fp8_channel_scales(inp: Inputs) -> np.ndarray:
+    """Per-channel scales of the FP8 cache, one per column of the 576-wide row (the
+    fine-grained per-channel scaling the Huny's Dev Blog page asks for in section 6,
+    item 4): s[d] = max over every cached token |row[d]| / 448, float32 (1 where the
+    column is all zero), so each column's largest value maps to the largest e4m3."""
+    amax = np.concatenate([np.abs(bf16_to_f32(inp.c)).max(axis=0), np.abs(bf16_to_f32(inp.kr)).max(axis=0)])
+    s = (amax.astype(np.float32) / np.float32(E4M3_MAX)).astype(np.float32)
+    s[s == 0] = np.float32(1.0)
+    return s
+
+
+def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to e4m3 codes (uint8): nearest, ties to even, magnitudes
+    beyond 448 saturated to 448, NaN -> 0x7F. e4m3: sign, 4 exponent bits (bias 7),
+    3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9; 0x7F / 0xFF are
+    NaN and there is no infinity. Rounding is done in float64, where dividing by the
+    quantum (a power of two) is exact."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(x)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, e2 = np.frexp(a)                       # a = f * 2^e2, f in [0.5, 1)
+    e = np.clip(e2 - 1, -6, 8)                # binade exponent (subnormals share -6)
+    quantum = np.ldexp(1.0, e - 3)            # 3 mantissa bits
+    v = np.round(a / quantum) * quantum       # numpy rounds halves to even
+    v = np.minimum(v, E4M3_MAX)
+    # encode the rounded magnitude
+    _, ev = np.frexp(v)
+    eb = np.clip(ev - 1, -6, 8)
+    normal = v >= 2.0 ** -6
+    mant = np.where(normal, v / np.ldexp(1.0, eb) - 1.0, v / 2.0 ** -9)
+    mbits = np.where(normal, np.round(mant * 8.0), np.round(mant)).astype(np.int64)
+    ebits = np.where(normal, eb + 7, 0).astype(np.int64)
+    code = (ebits << 3) | mbits
+    code = code | (sign.astype(np.int64) << 7)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize_fp8(rows_bf16: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """e4m3 codes of bf16 rows [..., 576] with per-column scales: the float32 quotient
+    row / s (one correctly rounded division), then f32_to_e4m3."""
+    x = bf16_to_f32(rows_bf16).astype(np.float32) / np.asarray(scales, dtype=np.float32)
+    return f32_to_e4m3(x.astype(np.float32))
+
+
+E4M3_NAN = np.uint8(0x7F)
+
+
+@dataclass
+class PagedFP8:
+    cache: np.ndarray        # e4m3 codes [num_pages, PAGE, 576] (uint8)
+    scales: np.ndarray       # float32 [576]
+    block_table: np.ndarray  # int32 [B, max_pages]
+    num_pages: int
+    max_pages: int
+    page_size: int = PAGE
+
+
+def make_paged_fp8(inp: Inputs, pg: Paged, scales: np.ndarray | None = None) -> PagedFP8:
+    """The FP8 cache holding the same tokens in the same pages as ``pg``: every row
+    quantised with per-channel scales (fp8_channel_scales unless given); slack rows
+    and spare pages hold the e4m3 NaN code."""
+    s = fp8_channel_scales(inp) if scales is None else np.asarray(scales, dtype=np.float32)
+    rows = pg.cache.reshape(-1, D_ROW)
+    codes = quantize_fp8(rows, s)
+    codes[(rows[:, 0] == BF16_NAN)] = E4M3_NAN  # poisoned rows stay poisoned
+    return PagedFP8(cache=codes.reshape(pg.cache.shape), scales=s, block_table=pg.block_table,
+                    num_pages=pg.num_pages, max_pages=pg.max_pages, page_size=pg.page_size)
+
+
 def latent_query_inputs(T: int, H: int, d_q: int, seed: int, d_nope: int = D_NOPE):
     """Compressed query latents and the query up-projection for the query-side
     absorption (seeded, numpy PCG64 ``default_rng(seed)``), in draw order:

@@ -47,6 +47,10 @@ PINS = {
     "merge_w_comb_f64": "pinned: numpy per-head product; an identity output projection gives W_UV",
     "out_comb_f64": "pinned: equals out_proj_f64 followed by the output projection (associativity); "
                     "identity output projection gives out_proj_f64's heads side by side",
+    "e4m3_decode": "pinned: torch's float8_e4m3fn values for all 256 codes; 1.0, 448, 2^-9, NaN codes",
+    "dequant_fp8_f64": "pinned: the generator's quantiser round trip within e4m3's half-quantum bound",
+    "absorbed_fp8_f64": "pinned: equals absorbed_f64 bit for bit when the dequantised latents are the bf16 "
+                        "inputs (scale 1, e4m3-exact values)",
 }
 
 
@@ -367,3 +371,56 @@ def out_comb_f64(u_bits, w_comb):
                                           ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     L.mla_oracle_out_comb_f64(_p(u), _p(w), T, H, d_c, d_model, _p(out))
     return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of e4m3 codes (uint8), from the format's definition (NaN codes -> NaN)."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.mla_oracle_e4m3_decode.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    lib.mla_oracle_e4m3_decode(_p(c), c.size, _p(out))
+    return out
+
+
+def dequant_fp8_f64(codes, scales) -> np.ndarray:
+    """Dequantised FP8 rows: codes [..., D] (uint8) times per-column scales [D] (float32), fp64."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    D = c.shape[-1]
+    assert sc.shape == (D,)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib.mla_oracle_dequant_fp8_f64.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_void_p]
+    lib.mla_oracle_dequant_fp8_f64(_p(c), _p(sc), c.size // D, D, _p(out))
+    return out
+
+
+def absorbed_lat_f64(inp, c, kr, rows=None, scale=None):
+    """absorbed_f64 with the latents given as float64 arrays c [total][d_c], kr [total][d_r]."""
+    lib = _load()
+    a, dims = _common(inp)
+    B, n_q, H, d_nope, d_r, d_c, d_v = dims
+    c = np.ascontiguousarray(c, dtype=np.float64)
+    kr = np.ascontiguousarray(kr, dtype=np.float64)
+    assert c.shape == (inp.total_tokens, d_c) and kr.shape == (inp.total_tokens, d_r)
+    rows = all_rows(inp) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    scale = default_scale(d_nope, d_r) if scale is None else scale
+    n = len(rows)
+    q_abs = np.empty((n, d_c + d_r)); u = np.empty((n, d_c)); lse = np.empty(n); out = np.empty((n, d_v))
+    rc = lib.mla_oracle_absorbed_lat_f64(
+        _p(a["q_nope"]), _p(a["q_rope"]), _p(c), _p(kr), _p(a["seq_off"]), _p(a["seq_lens"]),
+        _p(a["w_uk"]), _p(a["w_uv"]), *[ctypes.c_int(x) for x in dims], ctypes.c_double(scale),
+        _p(rows), ctypes.c_int64(n), _p(q_abs), _p(u), _p(lse), _p(out))
+    if rc != 0:
+        raise ValueError("oracle: bad row or context shorter than n_q")
+    return dict(q_abs=q_abs, u=u, lse=lse, out=out)
+
+
+def absorbed_fp8_f64(inp, codes, scales, rows=None, scale=None):
+    """The absorbed path on an FP8 latent cache: the logical rows' e4m3 codes [total][576]
+    dequantised with the per-column scales, then the exact fp64 absorbed loops."""
+    d_c = inp.c.shape[-1]
+    deq = dequant_fp8_f64(codes, scales)
+    return absorbed_lat_f64(inp, deq[:, :d_c], deq[:, d_c:], rows, scale)

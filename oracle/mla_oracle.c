@@ -607,3 +607,101 @@ int mla_oracle_append_f64(const uint16_t* h, const uint16_t* w_dkr, const int64_
     return 0;
 }
 
+
+/* ---------------------------------------------------------------- FP8 (e4m3) latents */
+/* An FP8 latent cache stores every row as e4m3 codes with one float32 scale per
+ * column (the per-channel scaling of Huny's Dev Blog section 6, item 4): the
+ * value of code q in column d is scale[d] * e4m3(q). e4m3 (the OCP 8-bit
+ * floating-point format): bit 7 sign, bits 6..3 exponent with bias 7, bits 2..0
+ * mantissa; exponent field 0 encodes the subnormals (m/8) * 2^-6; the codes with
+ * all exponent and mantissa bits set (0x7F, 0xFF) are NaN; there is no infinity. */
+static double e4m3_value(uint8_t q) {
+    const int sign = (q >> 7) & 1, ex = (q >> 3) & 15, man = q & 7;
+    double v;
+    if (ex == 15 && man == 7) return NAN;
+    if (ex == 0)
+        v = ldexp((double)man / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)man / 8.0, ex - 7);
+    return sign ? -v : v;
+}
+
+int mla_oracle_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(codes[i]);
+    return 0;
+}
+
+/* out[r][d] = scale[d] * e4m3(codes[r][d]) for rows r < n_rows, columns d < D. */
+int mla_oracle_dequant_fp8_f64(const uint8_t* codes, const float* scale, int64_t n_rows, int D, double* out) {
+    for (int64_t r = 0; r < n_rows; ++r)
+        for (int d = 0; d < D; ++d) out[r * D + d] = (double)scale[d] * e4m3_value(codes[r * D + d]);
+    return 0;
+}
+
+/* The absorbed path of mla_oracle_absorbed_f64 on latents given as doubles
+ * (c [total][d_c], kr [total][d_r], e.g. dequantised FP8 rows); queries and
+ * weights are bf16 bit patterns as there. Same loops, same order. */
+int mla_oracle_absorbed_lat_f64(const uint16_t* q_nope, const uint16_t* q_rope,
+                                const double* c, const double* kr,
+                                const int64_t* seq_off, const int32_t* seq_lens,
+                                const uint16_t* w_uk, const uint16_t* w_uv,
+                                int B, int n_q, int H, int d_nope, int d_r, int d_c, int d_v,
+                                double scale, const int64_t* rows, int64_t n_rows,
+                                double* q_abs_out, double* u_out, double* lse_out, double* out_out) {
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t ri = 0; ri < n_rows; ++ri) {
+        int64_t r = rows[ri];
+        int h = (int)(r % H);
+        int j = (int)((r / H) % n_q);
+        int b = (int)(r / ((int64_t)H * n_q));
+        if (b < 0 || b >= B) { bad = 1; continue; }
+        int64_t n_att = (int64_t)seq_lens[b] - n_q + j + 1;
+        if (n_att < 1) { bad = 1; continue; }
+        const uint16_t* qn = q_nope + r * d_nope;
+        const uint16_t* qr = q_rope + r * d_r;
+        const uint16_t* wk = w_uk + (int64_t)h * d_nope * d_c;
+        const uint16_t* wv = w_uv + (int64_t)h * d_v * d_c;
+        const double* cb = c + seq_off[b] * d_c;
+        const double* kb = kr + seq_off[b] * d_r;
+        double* qt = (double*)calloc((size_t)d_c, sizeof(double));
+        double* z = (double*)malloc((size_t)n_att * sizeof(double));
+        double* u = (double*)calloc((size_t)d_c, sizeof(double));
+        for (int i = 0; i < d_nope; ++i) {
+            double qi = bf(qn[i]);
+            for (int cc = 0; cc < d_c; ++cc) qt[cc] += qi * bf(wk[(int64_t)i * d_c + cc]);
+        }
+        double m = -INFINITY;
+        for (int64_t s = 0; s < n_att; ++s) {
+            double content = 0.0, pos = 0.0;
+            for (int cc = 0; cc < d_c; ++cc) content += qt[cc] * cb[s * d_c + cc];
+            for (int e = 0; e < d_r; ++e) pos += bf(qr[e]) * kb[s * d_r + e];
+            z[s] = (content + pos) * scale;
+            if (z[s] > m) m = z[s];
+        }
+        double l = 0.0;
+        for (int64_t s = 0; s < n_att; ++s) l += exp(z[s] - m);
+        for (int64_t s = 0; s < n_att; ++s) {
+            double p = exp(z[s] - m) / l;
+            for (int cc = 0; cc < d_c; ++cc) u[cc] += p * cb[s * d_c + cc];
+        }
+        if (q_abs_out) {
+            double* qa = q_abs_out + ri * (d_c + d_r);
+            for (int cc = 0; cc < d_c; ++cc) qa[cc] = qt[cc];
+            for (int e = 0; e < d_r; ++e) qa[d_c + e] = bf(qr[e]);
+        }
+        if (u_out) memcpy(u_out + ri * d_c, u, (size_t)d_c * sizeof(double));
+        if (lse_out) lse_out[ri] = m + log(l);
+        if (out_out) {
+            for (int i = 0; i < d_v; ++i) {
+                double acc = 0.0;
+                for (int cc = 0; cc < d_c; ++cc) acc += bf(wv[(int64_t)i * d_c + cc]) * u[cc];
+                out_out[ri * d_v + i] = acc;
+            }
+        }
+        free(qt);
+        free(z);
+        free(u);
+    }
+    return bad ? -1 : 0;
+}
