@@ -402,6 +402,27 @@ def run_ours(args):
     append_us = per_call_us(append)
     latent_us = per_call_us(absorb_latent)
     comb_us = per_call_us(out_comb)
+
+    # FP8 latent cache (e4m3 codes, per-column scales): the same pages quantised on the
+    # device, then the planned decode call on them, timed like the bf16 one
+    fp8_scales = torch.from_numpy(mi.fp8_channel_scales(inp)).to(dev)
+    for S in sets:
+        S["cache8"] = mla.quantize_fp8(S["cache"], fp8_scales)
+
+    def quantize8(S):
+        mla.quantize_fp8(S["cache"], fp8_scales, S["cache8"])
+
+    def decode8_planned(S):
+        mla.decode_paged_fp8(S["q_abs"], S["cache8"], fp8_scales, S["bt"], S["sl"], n_q=n_q, num_splits=G,
+                             workspace=S["workspace"], err_word=err, planned=True)
+
+    for k in range(NSETS):
+        plan(sets[k])
+    fp8_dec_us = per_call_us(decode8_planned)
+    fp8_quant_us = per_call_us(quantize8)
+    for k in range(NSETS):
+        plan(sets[k])
+        decode_planned(sets[k])  # the bf16 partials back in the workspaces
     # for reference: one step replayed alone after an L2 flush (cold caches,
     # including the graph launch, about 6.6 us on this system)
     g1 = capture(lambda: step(sets[0]))
@@ -476,6 +497,7 @@ def run_ours(args):
             "append_kv": append_line(append_us, T, hbm),
             "absorb_q_latent": latent_line(latent_us, phases["absorb_q"], T, H, hbm),
             "out_comb": comb_line(comb_us, phases["out_proj"], T, H, hbm),
+            "fp8_decode": fp8_line(fp8_dec_us, fp8_quant_us, inp, hbm, tflops, src, dec_us),
             "gpu_launches": 5 * args.steps,
             "timing": (f"CUDA events around the timed region: graphs of {R} back-to-back steps over "
                        f"{NSETS} rotating input sets, replayed until {args.steps} steps ran"),
@@ -571,6 +593,23 @@ def side_workloads(mla, dev, err, hbm, tflops, src, exclude=None, calls=20, reps
         del S, bufs
         torch.cuda.empty_cache()
     return res
+
+
+def fp8_line(us, quant_us, inp, hbm, tflops, src, bf16_us):
+    """The decode kernel on the FP8 cache (e4m3 codes, one float scale per column): its time
+    per call and roofline. The cache bytes halve, so the flops per byte double (past the
+    ridge point of the measured peaks: tensor bound). quantize_us: the whole cache quantised
+    once (151 MB read, 75 MB written), for context."""
+    T, H = inp.B * inp.n_q, inp.H
+    wb = mi.workload_bytes(inp)
+    cache8 = int(inp.seq_lens.sum()) * 576
+    nbytes = cache8 + T * H * 576 * 2 + inp.B * 4 + int(mi.pages_for(inp.seq_lens).sum()) * 4 + 576 * 4
+    return {"kernel": "mla_decode_paged_planned_fp8", "decode_us": us, "cache_bytes": cache8,
+            "cache_bytes_bf16": wb["cache_bytes"], "alg_bytes_per_launch": nbytes,
+            "alg_flops_per_launch": wb["decode_flops"],
+            **roofline_bound(wb["decode_flops"], nbytes, us, hbm, tflops), "peak_source": src,
+            "speedup_vs_bf16_decode": bf16_us / us, "quantize_us": quant_us,
+            "duration": "per call, back to back over the rotating input sets"}
 
 
 def append_line(us, T, hbm):

@@ -259,6 +259,47 @@ mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache
                                     float softmax_scale, int num_splits, void* workspace, size_t workspace_bytes,
                                     int32_t* err_word, void* stream);
 
+/* ------------------------------------------------------------------------
+ * FP8 latent cache (Huny's Dev Blog section 6, item 4: FP8 on the latent cache
+ * needs fine-grained per-channel or per-block scale factors, not one per
+ * tensor, or outliers cost accuracy; ailab.paldyn.com "MQA와 GQA", KV-cache
+ * quantisation: 1 byte per value halves the cache, and K's outlier channels are
+ * why it is scaled per channel). A cached row is 576 e4m3 codes (1 byte each,
+ * 576 bytes per token) with one float32 scale per column, shared by every token
+ * of the cache: value = scales[d] * e4m3(code). e4m3: sign bit, 4 exponent bits
+ * (bias 7), 3 mantissa bits, subnormals at exponent 0, 0x7F / 0xFF NaN, no
+ * infinity, largest finite value 448.
+ *
+ * mla_quantize_fp8 — codes of bf16 rows with given scales:
+ *   codes[r][d] = e4m3(rows[r][d] / scales[d])
+ * the quotient one correctly rounded fp32 division, the conversion nearest
+ * (ties to even) and saturating at +-448.
+ *   rows [n_rows][576] bf16 (a paged cache is rows [num_pages * page_size][576]),
+ *   scales [576] float32 (> 0), codes [n_rows][576] uint8 (output).
+ *
+ * mla_decode_paged_fp8 / mla_decode_paged_planned_fp8 — mla_decode_paged /
+ * mla_decode_paged_planned on an FP8 cache: the same partials in the same
+ * workspace (merged by mla_combine), computed on the dequantised latents
+ *   row_s[d] = scales[d] * e4m3(cache8[block_table[b][s / 64]][s % 64][d]).
+ * Each code is read from HBM once. The scales are folded into the query (the
+ * scores) and into the written partials (the values); the codes are widened to
+ * fp16 in shared memory (exactly) and the MMAs take fp16 operands (the scaled
+ * query, P and the page), fp32 accumulation.
+ *   cache8 [num_pages][page_size][576] uint8, scales [576] float32; the other
+ *   arguments, the ordering rule and the error reporting are those of
+ *   mla_decode_paged / mla_decode_paged_planned. */
+mla_status mla_quantize_fp8(const uint16_t* rows, const float* scales, uint8_t* codes, int64_t n_rows,
+                            void* stream);
+mla_status mla_decode_paged_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* scales,
+                                const int32_t* block_table, const int32_t* seq_lens, int B, int n_q, int H,
+                                int num_pages, int page_size, int max_pages_per_seq, float softmax_scale,
+                                int num_splits, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                void* stream);
+mla_status mla_decode_paged_planned_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* scales,
+                                        const int32_t* block_table, int B, int n_q, int H, int num_pages,
+                                        int page_size, int max_pages_per_seq, float softmax_scale, int num_splits,
+                                        void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream);
+
 /* mla_combine — merge the range partials of each (sequence, query, head):
  *   lse = ln sum_k exp(lse_k),  u = sum_k exp(lse_k - lse) * o_k
  * (the flash-decoding merge; Huny's Dev Blog section 4 table names

@@ -303,6 +303,7 @@ def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
     eb = np.clip(ev - 1, -6, 8)
     normal = v >= 2.0 ** -6
     mant = np.where(normal, v / np.ldexp(1.0, eb) - 1.0, v / 2.0 ** -9)
+    mant = np.nan_to_num(mant)  # NaN inputs get their code below
     mbits = np.where(normal, np.round(mant * 8.0), np.round(mant)).astype(np.int64)
     ebits = np.where(normal, eb + 7, 0).astype(np.int64)
     code = (ebits << 3) | mbits

@@ -46,6 +46,7 @@ EXPORTS = [
     "mla_append_workspace_bytes", "mla_append_kv",
     "mla_merge_w_kq", "mla_absorb_q_latent",
     "mla_merge_w_comb", "mla_out_comb_workspace_bytes", "mla_out_comb",
+    "mla_quantize_fp8", "mla_decode_paged_fp8", "mla_decode_paged_planned_fp8",
 ]
 
 
@@ -142,6 +143,12 @@ def _load(path: str):
     L.mla_out_comb_workspace_bytes.argtypes = [i, i, i]
     L.mla_out_comb.restype = i
     L.mla_out_comb.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
+    L.mla_quantize_fp8.restype = i
+    L.mla_quantize_fp8.argtypes = [vp, vp, vp, ctypes.c_int64, vp]
+    L.mla_decode_paged_fp8.restype = i
+    L.mla_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
+    L.mla_decode_paged_planned_fp8.restype = i
+    L.mla_decode_paged_planned_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
     return L
 
 
@@ -331,6 +338,50 @@ def combine(workspace, *, B: int, n_q: int, H: int, num_splits: int, u=None, lse
                            _stream(stream))
     _check(st, "mla_combine")
     return u, lse
+
+
+def quantize_fp8(rows, scales, codes=None, stream=None):
+    """e4m3 codes of bf16 rows [..., 576] with per-column scales [576] float32 (FP8 latent cache)."""
+    import torch
+    if codes is None:
+        codes = torch.empty(rows.shape, dtype=torch.uint8, device=rows.device)
+    assert scales.dtype == torch.float32 and scales.is_contiguous() and scales.numel() == D_ROW
+    n_rows = rows.numel() // D_ROW
+    st = lib().mla_quantize_fp8(_ptr(_bits(rows)), _ptr(scales), _ptr(codes), n_rows, _stream(stream))
+    _check(st, "mla_quantize_fp8")
+    return codes
+
+
+def decode_paged_fp8(q_abs, cache8, scales, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
+                     softmax_scale: float = DEFAULT_SCALE, workspace=None, err_word=None, stream=None,
+                     planned: bool = False):
+    """decode_paged on an FP8 cache: cache8 [num_pages, 64, 576] uint8 e4m3 codes, scales [576]
+    float32 per column. Returns (workspace, num_splits) for ``combine``."""
+    import torch
+    B, max_pages = block_table.shape
+    H = q_abs.shape[-2]
+    num_pages, page_size = cache8.shape[0], cache8.shape[1]
+    if num_splits is None:
+        num_splits = default_splits(n_q)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(B, n_q, H, num_splits), dtype=torch.uint8, device=q_abs.device)
+    assert cache8.dtype == torch.uint8 and cache8.is_contiguous()
+    assert scales.dtype == torch.float32 and scales.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.is_contiguous()
+    nb = workspace.numel() * workspace.element_size()
+    if planned:
+        st = lib().mla_decode_paged_planned_fp8(_ptr(_bits(q_abs)), _ptr(cache8), _ptr(scales), _ptr(block_table),
+                                                B, n_q, H, num_pages, page_size, max_pages, float(softmax_scale),
+                                                num_splits, _ptr(workspace), nb, _ptr(err_word), _stream(stream))
+        _check(st, "mla_decode_paged_planned_fp8")
+    else:
+        assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+        st = lib().mla_decode_paged_fp8(_ptr(_bits(q_abs)), _ptr(cache8), _ptr(scales), _ptr(block_table),
+                                        _ptr(seq_lens), B, n_q, H, num_pages, page_size, max_pages,
+                                        float(softmax_scale), num_splits, _ptr(workspace), nb, _ptr(err_word),
+                                        _stream(stream))
+        _check(st, "mla_decode_paged_fp8")
+    return workspace, num_splits
 
 
 def decode_noalloc(q_abs, cache, block_table, seq_lens, *, n_q: int, u, lse=None, num_splits: int | None = None,

@@ -72,6 +72,15 @@ constexpr uint32_t kPPeerBytes = 128 * 64;  // the peer's half of P: [128 heads]
 constexpr uint32_t kPHalfBytes = kPPeerBytes;
 constexpr int kPBufs = 3;  // P buffers: page g uses g % 3, so its writers wait for page g - 3
 constexpr uint32_t kTokBytes = 4 * 4;       // "partial consumed" tokens: one per warp of a group
+// FP8 cache: a CTA's half of a page (e4m3 codes, [64 tokens][256 latent + 32
+// positional columns], rows of 64 and 32 bytes) lands in the upper half of its
+// ring slot, and the score readers expand it in place into the layout of the
+// 16-bit page half above (fp16 values: e4m3 converts to fp16 exactly).
+constexpr uint32_t kF8CBoxBytes = 64 * 64;   // [64 tokens][64 latent cols] e4m3
+constexpr uint32_t kF8KrBoxBytes = 64 * 32;  // [64 tokens][32 positional cols] e4m3
+constexpr uint32_t kF8StageBytes = 4 * kF8CBoxBytes + kF8KrBoxBytes;  // 18432
+constexpr uint32_t kF8Off = kStageBytes - kF8StageBytes;              // 18432
+constexpr int kF8Chunks = kF8StageBytes / 16;  // 16-byte chunks of a page half: 1152
 
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffX = kOffStage + kStages * kStageBytes;  // peer partial scores, one buffer per group
@@ -93,7 +102,11 @@ enum {
   SF0 = QCF + 1, SFREE = SF0 + 2, PF0 = SFREE + 1, PVD0 = PF0 + kPBufs, XF0 = PVD0 + kPBufs, XE0 = XF0 + 2,
   MXF0 = XE0 + 2, LXF0 = MXF0 + 2, MRF = LXF0 + 2, LGF0 = MRF + 1, IVF0 = LGF0 + 2, OFREE = IVF0 + 2,
   MMAD = OFREE + 1,
-  kNumBars = MMAD + 1
+  // FP8 cache only: CVF = a ring slot's 16-bit page half (or query) is in place
+  // (every use of a slot completes it once, so its phases follow FULL's); CVR =
+  // every score reader has read its share of the codes of the page being expanded
+  CVF0 = MMAD + 1, CVR = CVF0 + kStages,
+  kNumBars = CVR + 1
 };
 constexpr uint32_t kOffSlots = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffSlots + 16;  // the base is checked to be 1024-byte aligned
@@ -132,11 +145,35 @@ __device__ __noinline__ bool dbg_check(bool ok, int32_t* err_word) {
 #endif
 
 
+// kF8: the cache holds e4m3 codes with a scale per column (fp8_scales, 576
+// floats). The scales are folded into the query (scores) and into the written
+// partials (values), the codes are expanded to fp16 in shared memory, and the
+// MMAs run on fp16 operands (the query, P and the page, kind::f16 with fp16
+// inputs); the bf16 path is unchanged.
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// Four e4m3 codes (byte i = value i) -> fp16 pairs: values 0,1 in lo, 2,3 in hi
+// (exact: every e4m3 value is an fp16 value).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// bf16 pair times two scales, as an fp16 pair
+__device__ __forceinline__ uint32_t scale_bf16x2_to_f16x2(uint32_t w, float s0, float s1) {
+  return cvt_f16x2(bf16_lo(w) * s0, bf16_hi(w) * s1);
+}
+
+template <bool kF8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
                  const __grid_constant__ CUtensorMap map_qkr, const __grid_constant__ CUtensorMap map_q,
                  const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, int num_pages,
-                 float sl2, Plan plan, int32_t* err_word) {
+                 float sl2, Plan plan, const float* __restrict__ fp8_scales, int32_t* err_word) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -176,6 +213,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     mbar_init(bar(QCF), kAThreads);  // the range's latent query half is in tensor memory
     mbar_init(bar(OFREE), 2 * kGThreads);        // both halves of O drained
     mbar_init(bar(MMAD), 2);  // both MMA issuers done
+    if (kF8) {
+      for (int i = 0; i < kStages; ++i) mbar_init(bar(CVF0 + i), kAThreads);
+      mbar_init(bar(CVR), kAThreads);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     for (int i = 0; i < kPBufs; ++i) mbar_arrive_expect_tx(bar(PF0 + i), kPHalfBytes);
@@ -281,12 +322,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       if (lane == 0 && MLA_SMEM_OK(sbase + kOffStage + stage * kStageBytes, kStageBytes)) {
         const uint32_t fb = bar(FULL0 + stage);
         const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
-        mbar_arrive_expect_tx(fb, kStageBytes);
         const int y = pid * kPage;
+        if (kF8) {
+          // the codes into the upper half of the slot, unswizzled rows
+          mbar_arrive_expect_tx(fb, kF8StageBytes);
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb)
-          tma_load_2d(dst + cb * kCBoxBytes, &map_c, fb, 256 * (int)rank + 64 * cb, y, pol_stream);
-        tma_load_2d(dst + 4 * kCBoxBytes, &map_kr, fb, kDC + 32 * (int)rank, y, pol_stream);
+          for (int cb = 0; cb < 4; ++cb)
+            tma_load_2d(dst + kF8Off + cb * kF8CBoxBytes, &map_c, fb, 256 * (int)rank + 64 * cb, y, pol_stream);
+          tma_load_2d(dst + kF8Off + 4 * kF8CBoxBytes, &map_kr, fb, kDC + 32 * (int)rank, y, pol_stream);
+        } else {
+          mbar_arrive_expect_tx(fb, kStageBytes);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+            tma_load_2d(dst + cb * kCBoxBytes, &map_c, fb, 256 * (int)rank + 64 * cb, y, pol_stream);
+          tma_load_2d(dst + 4 * kCBoxBytes, &map_kr, fb, kDC + 32 * (int)rank, y, pol_stream);
+        }
       }
       last_ph[stage] = (int)ph;
       __syncwarp();
@@ -312,8 +362,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     // follows that page's score MMAs through S -> P, so its commit (EMPTY)
     // also covers the page's score MMAs.
     if (lane == 0) {
-      constexpr uint32_t kIdQK = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(128, 256, false, true);
+      constexpr uint32_t kIdQK = kF8 ? idesc_f16(128, 64, false, false) : idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdPV = kF8 ? idesc_f16(128, 256, false, true) : idesc_bf16(128, 256, false, true);
       // descriptor templates; the start address is added per use
       const uint64_t dQK_c = smem_desc(0, 16, 1024, kSwizzle128B);
       const uint64_t dQK_r = smem_desc(0, 16, 512, kSwizzle64B);
@@ -340,7 +390,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           }
           for (int i = 0; i < ntiles; ++i, ++g) {
-            if (!wait_phase(bar(FULL0 + stage), ph, abort_flag, err_word) ||
+            // an FP8 page is expanded by the score readers after it lands (CVF)
+            if (!wait_phase(bar((kF8 ? CVF0 : FULL0) + stage), ph, abort_flag, err_word) ||
                 !wait_phase(bar(SFREE), (g & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d = tmem + kTmS;
@@ -416,6 +467,65 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       const uint32_t tQ = tmem + lane_off + kTmQ;
       int g = 0;
       bool ok = true;
+      // FP8 cache: expand the codes of page gg (range li) in place into the fp16
+      // page half the MMAs read. Every reader first loads its 9 of the 1152
+      // 16-byte chunks (the codes sit in the upper half of the slot, which the
+      // expansion overwrites), all readers meet (CVR), then each writes its
+      // chunks' 16 values as two 16-byte chunks of the swizzled layout of the
+      // TMA boxes of the bf16 path. Pages are expanded in order, at most two
+      // ahead of the page whose scores are being read and never beyond the
+      // current range (the next range's query slots come first in the ring).
+      int cv_n = 0, cv_next = 0, cv_last = -1;
+      auto expand = [&](int gg, int lii) -> bool {
+        const int slot = gg + kQSlots * (lii + 1);
+        const int st = slot % kStages;
+        if (!wait_phase(bar(FULL0 + st), (slot / kStages) & 1, abort_flag, err_word)) return false;
+        const uint32_t sb = sbase + kOffStage + st * kStageBytes;
+        uint32_t v[9][4];
+#pragma unroll
+        for (int k = 0; k < 9; ++k)
+          ld_shared_v4(sb + kF8Off + (uint32_t)(atid + 128 * k) * 16, v[k][0], v[k][1], v[k][2], v[k][3]);
+        mbar_arrive(bar(CVR));
+        if (!wait_phase(bar(CVR), cv_n & 1, abort_flag, err_word)) return false;
+        ++cv_n;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const uint32_t q = (uint32_t)atid + 128u * k;
+          uint32_t a0, a1;
+          if (q < 1024) {  // latent box q / 256, token row, 16 of its 64 columns
+            const uint32_t cb = q >> 8, t = (q >> 2) & 63, kk = q & 3;
+            const uint32_t base = sb + cb * kCBoxBytes + t * 128;
+            a0 = base + (((2 * kk) ^ (t & 7)) * 16);
+            a1 = base + (((2 * kk + 1) ^ (t & 7)) * 16);
+          } else {  // positional box: token row, 16 of its 32 columns (64B swizzle)
+            const uint32_t qq = q - 1024, t = qq >> 1, kk = qq & 1;
+            const uint32_t base = sb + 4 * kCBoxBytes + t * 64;
+            a0 = base + (((2 * kk) ^ ((t >> 1) & 3)) * 16);
+            a1 = base + (((2 * kk + 1) ^ ((t >> 1) & 3)) * 16);
+          }
+          uint32_t o[8];
+          e4m3x4_to_f16(v[k][0], o[0], o[1]);
+          e4m3x4_to_f16(v[k][1], o[2], o[3]);
+          e4m3x4_to_f16(v[k][2], o[4], o[5]);
+          e4m3x4_to_f16(v[k][3], o[6], o[7]);
+          if (MLA_SMEM_OK(a0, 16) && MLA_SMEM_OK(a1, 16)) {
+            st_shared_v4(a0, o[0], o[1], o[2], o[3]);
+            st_shared_v4(a1, o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();  // read by the MMAs (async proxy)
+        mbar_arrive(bar(CVF0 + st));
+        return true;
+      };
+      auto expand_upto = [&](int target, int lii) -> bool {
+        if (target > cv_last) target = cv_last;
+        while (cv_next <= target) {
+          if (!expand(cv_next, lii)) return false;
+          ++cv_next;
+        }
+        return true;
+      };
+
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
         const int pg0 = plan.item_page0[it];
@@ -438,6 +548,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(r[4 * c]), "=r"(r[4 * c + 1]), "=r"(r[4 * c + 2]), "=r"(r[4 * c + 3])
                            : "r"(sq + m * kQBoxBytes + ((c ^ (row & 7)) * 16)));
+            if (kF8) {  // the FP8 cache's column scales fold into the query (fp16)
+              const float* sc = fp8_scales + 256 * rank + 128 * q + 64 * m;
+#pragma unroll
+              for (int k = 0; k < 32; ++k) r[k] = scale_bf16x2_to_f16x2(r[k], __ldg(sc + 2 * k), __ldg(sc + 2 * k + 1));
+            }
             tmem_st32(tQ + 64 * q + 32 * m, r);
           }
           if ((row >> 6) == q) {  // this row's positional half: 64 bytes, 64B-swizzled (warp-uniform)
@@ -449,13 +564,25 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(r[4 * c]), "=r"(r[4 * c + 1]), "=r"(r[4 * c + 2]), "=r"(r[4 * c + 3])
                            : "r"(sr + rl * 64 + ((c ^ ((rl >> 1) & 3)) * 16)));
+            if (kF8) {
+              const float* sc = fp8_scales + kDC + 32 * rank;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) r[k] = scale_bf16x2_to_f16x2(r[k], __ldg(sc + 2 * k), __ldg(sc + 2 * k + 1));
+            }
             tmem_st16(tmem + lane_off + kTmQr, r);
           }
+          // every use of a ring slot completes its CVF once (the query's too)
+          if (kF8) mbar_arrive(bar(CVF0 + slot % kStages));
         }
         if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(QCF));
+        if (kF8) {  // the range's first page, expanded before its score MMAs
+          cv_next = g;
+          cv_last = g + ntiles - 1;
+          if (!expand_upto(g, li)) { ok = false; break; }
+        }
         for (int i = 0; i < ntiles; ++i, ++g) {
           if (!wait_phase(bar(SF0 + (g & 1)), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
@@ -510,6 +637,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
             }
             st_async_b32(r_x + xoff + kXDataBytes + (uint32_t)row * 4, __float_as_uint(mid), xf);
           }
+          // FP8 cache: expand the range's pages up to two ahead of this one
+          if (kF8 && !expand_upto(g + 2, li)) { ok = false; break; }
         }
       }
     } else {
@@ -549,6 +678,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               f[e] = __uint_as_float(r[8 * v + e]) * inv;
+              // the FP8 cache's column scale (u = s * sum p code)
+              if (kF8) f[e] *= __ldg(fp8_scales + 256 * rank + 128 * half + 32 * c + 8 * v + e);
               amax = fmaxf(amax, fabsf(f[e]));
             }
             if (row < H)
@@ -711,9 +842,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           for (int v = 0; v < 16; ++v) {
             const float p0 = ex2(x[2 * v] - mref);
             const float p1 = ex2(x[2 * v + 1] - mref);
-            pw[v] = cvt_bf16x2(p0, p1);
-            lsum0 += bf16_lo(pw[v]);
-            lsum1 += bf16_hi(pw[v]);
+            if (kF8) {  // fp16 operands with the FP8 cache
+              pw[v] = cvt_f16x2(p0, p1);
+              const float2 f = f16x2_to_f32(pw[v]);
+              lsum0 += f.x;
+              lsum1 += f.y;
+            } else {
+              pw[v] = cvt_bf16x2(p0, p1);
+              lsum0 += bf16_lo(pw[v]);
+              lsum1 += bf16_hi(pw[v]);
+            }
           }
           tmem_st16(tmem + lane_off + kTmP + 16 * pb, pw);
 #pragma unroll
@@ -789,7 +927,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 
 // ---------------------------------------------------------------- host side
 int decode_max_workers() {
-  if (smem_limit<decode_tc_kernel>(kSmemBytes) != cudaSuccess) {
+  if (smem_limit<decode_tc_kernel<false>>(kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return -1;
   }
@@ -805,32 +943,63 @@ int decode_max_workers() {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return -1;
   }
   return n;
 }
 
-cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
-                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
-                          const Plan& plan, int32_t* err_word, cudaStream_t s) {
-  CUtensorMap map_c, map_kr, map_qkr, map_q;
-  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+namespace {
+// The query maps and the launch, shared by the bf16 and FP8 caches (the page
+// maps differ: 16-bit swizzled boxes, or unswizzled 8-bit rows).
+template <bool kF8>
+cudaError_t launch_decode_impl(const CUtensorMap& map_c, const CUtensorMap& map_kr, const uint16_t* q_abs,
+                               const float* fp8_scales, const int32_t* block_table, int B, int n_q, int H,
+                               int num_pages, int max_pages, float scale, int G, const Plan& plan, int32_t* err_word,
+                               cudaStream_t s) {
+  CUtensorMap map_qkr, map_q;
   const uint64_t q_dims[2] = {kRow, (uint64_t)B * n_q * H};
   const uint64_t row_stride[1] = {kRow * 2};
-  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64}, box_qkr[2] = {32, 64}, box_q[2] = {64, 128};
-  if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
-      !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64) ||
-      !make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64) ||
+  const uint32_t box_qkr[2] = {32, 64}, box_q[2] = {64, 128};
+  if (!make_tmap(&map_qkr, q_abs, 2, q_dims, row_stride, box_qkr, 64) ||
       !make_tmap(&map_q, q_abs, 2, q_dims, row_stride, box_q, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = smem_limit<decode_tc_kernel>(kSmemBytes);
+  cudaError_t e = smem_limit<decode_tc_kernel<kF8>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const float sl2 = scale * 1.4426950408889634f;
   dim3 grid(2 * G, n_q, 1);
-  return launch_pdl(decode_tc_kernel, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, map_q,
-                    block_table, n_q, H, max_pages, num_pages, sl2, plan, err_word);
+  return launch_pdl(decode_tc_kernel<kF8>, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, map_q,
+                    block_table, n_q, H, max_pages, num_pages, sl2, plan, fp8_scales, err_word);
+}
+}  // namespace
+
+cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
+                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
+                          const Plan& plan, int32_t* err_word, cudaStream_t s) {
+  CUtensorMap map_c, map_kr;
+  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+  const uint64_t row_stride[1] = {kRow * 2};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64};
+  if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
+      !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64))
+    return cudaErrorInvalidValue;
+  return launch_decode_impl<false>(map_c, map_kr, q_abs, nullptr, block_table, B, n_q, H, num_pages, max_pages,
+                                   scale, G, plan, err_word, s);
+}
+
+cudaError_t launch_decode_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* fp8_scales,
+                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int max_pages,
+                              float scale, int G, const Plan& plan, int32_t* err_word, cudaStream_t s) {
+  CUtensorMap map_c, map_kr;
+  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+  const uint64_t row_stride[1] = {kRow};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64};
+  if (!make_tmap(&map_c, cache8, 2, cache_dims, row_stride, box_c, 0, true) ||
+      !make_tmap(&map_kr, cache8, 2, cache_dims, row_stride, box_kr, 0, true))
+    return cudaErrorInvalidValue;
+  return launch_decode_impl<true>(map_c, map_kr, q_abs, fp8_scales, block_table, B, n_q, H, num_pages, max_pages,
+                                  scale, G, plan, err_word, s);
 }
 
 }  // namespace mla

@@ -172,6 +172,53 @@ mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                                      max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
 }
 
+mla_status mla_quantize_fp8(const uint16_t* rows, const float* scales, uint8_t* codes, int64_t n_rows,
+                            void* stream) {
+  if (!rows || !scales || !codes) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(rows) || !aligned16(scales) || !aligned16(codes)) return MLA_ERR_INVALID_ARG;
+  if (n_rows < 1 || n_rows > ((int64_t)1 << 40)) return MLA_ERR_INVALID_ARG;
+  return launch_status(launch_quantize_fp8(rows, scales, codes, n_rows, (cudaStream_t)stream));
+}
+
+mla_status mla_decode_paged_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* scales,
+                                const int32_t* block_table, const int32_t* seq_lens, int B, int n_q, int H,
+                                int num_pages, int page_size, int max_pages_per_seq, float softmax_scale,
+                                int num_splits, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                void* stream) {
+  if (!q_abs || !cache8 || !scales || !block_table || !seq_lens) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache8) || !aligned16(scales) || !aligned16(block_table) ||
+      !aligned16(seq_lens))
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
+  Plan plan;
+  mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
+                              num_splits, &plan);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
+                                 err_word, s));
+  if (st != MLA_OK) return st;
+  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages,
+                                         max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
+}
+
+mla_status mla_decode_paged_planned_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* scales,
+                                        const int32_t* block_table, int B, int n_q, int H, int num_pages,
+                                        int page_size, int max_pages_per_seq, float softmax_scale, int num_splits,
+                                        void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+  if (!q_abs || !cache8 || !scales || !block_table) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache8) || !aligned16(scales) || !aligned16(block_table))
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
+  Plan plan;
+  mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
+                              num_splits, &plan);
+  if (st != MLA_OK) return st;
+  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages,
+                                         max_pages_per_seq, softmax_scale, num_splits, plan, err_word,
+                                         (cudaStream_t)stream));
+}
+
 mla_status mla_decode_plan(const int32_t* seq_lens, int B, int n_q, int H, int num_pages, int page_size,
                            int max_pages_per_seq, int num_splits, void* workspace, size_t workspace_bytes,
                            int32_t* err_word, void* stream) {

@@ -91,10 +91,10 @@ __device__ inline uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- tensor maps
-// bf16 tensor map of `rank` dims (dims[0] innermost), byte strides of dims
-// 1..rank-1, box extents, swizzle span in bytes (0, 32, 64 or 128).
+// bf16 (or, with u8, 8-bit) tensor map of `rank` dims (dims[0] innermost), byte
+// strides of dims 1..rank-1, box extents, swizzle span in bytes (0, 32, 64 or 128).
 bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box, int swizzle_bytes);
+               const uint32_t* box, int swizzle_bytes, bool u8 = false);
 
 // ---------------------------------------------------------------- launch helper
 // Launch with programmatic stream serialization: the kernel may start while
@@ -143,6 +143,14 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
                           int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s);
+// The same decode over an FP8 cache: e4m3 codes [num_pages][64][576] and one
+// float scale per column (fp8_scales[576]).
+cudaError_t launch_decode_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* fp8_scales,
+                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int max_pages,
+                              float scale, int G, const Plan& plan, int32_t* err_word, cudaStream_t s);
+// e4m3 codes of bf16 rows of 576 values with per-column scales
+cudaError_t launch_quantize_fp8(const uint16_t* rows, const float* scales, uint8_t* codes, int64_t n_rows,
+                                cudaStream_t s);
 // Worker clusters (CTA pairs) of the decode kernel that fit on the device at once.
 int decode_max_workers();
 cudaError_t launch_combine(const Plan& plan, int B, int n_q, int H, uint16_t* u, float* lse,

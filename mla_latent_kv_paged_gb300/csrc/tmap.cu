@@ -1,4 +1,4 @@
-// Host-side construction of TMA tensor maps (bf16, row-major tensors). The
+// Host-side construction of TMA tensor maps (bf16 or 8-bit, row-major tensors). The
 // driver entry point is fetched through the runtime, so the library has no
 // link-time dependency on the driver library.
 #include <cudaTypedefs.h>
@@ -33,7 +33,7 @@ CUtensorMapSwizzle swizzle_mode(int bytes) {
 }  // namespace
 
 bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box, int swizzle_bytes) {
+               const uint32_t* box, int swizzle_bytes, bool u8) {
   auto fn = encode_fn();
   if (!fn || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], st[4];
@@ -44,7 +44,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     es[i] = 1;
     if (i > 0) st[i - 1] = strides_bytes[i - 1];
   }
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
+  return fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_mode(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

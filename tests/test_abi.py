@@ -300,3 +300,37 @@ def test_plan_switch_cost_dropped_when_steps_are_short():
     assert plan_mirror([1] * 4096, 1, 4, 76)["switch"] == 3
     pl = plan_mirror([1] * 3, 1, 4, 3)
     assert pl["switch"] == 0 and len(pl["items"]) == 3
+
+
+def test_host_validation_fp8(lib):
+    p = FAKE
+    assert lib.mla_quantize_fp8(None, p, p, 4, None) == 1
+    assert lib.mla_quantize_fp8(p, p + 4, p, 4, None) == 1
+    assert lib.mla_quantize_fp8(p, p, p, 0, None) == 1
+    ws = lib.mla_decode_workspace_bytes(2, 1, 16, 4)
+
+    def dec(**kw):
+        a = dict(q=p, cache=p, s=p, bt=p, sl=p, B=2, n_q=1, H=16, num_pages=8, page=64, maxp=4,
+                 scale=0.07, G=4, ws=p, wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_decode_paged_fp8(a["q"], a["cache"], a["s"], a["bt"], a["sl"], a["B"], a["n_q"], a["H"],
+                                        a["num_pages"], a["page"], a["maxp"], a["scale"], a["G"], a["ws"], a["wsb"],
+                                        a["err"], None)
+
+    def planned(**kw):
+        a = dict(q=p, cache=p, s=p, bt=p, B=2, n_q=1, H=16, num_pages=8, page=64, maxp=4, scale=0.07, G=4, ws=p,
+                 wsb=ws, err=None)
+        a.update(kw)
+        return lib.mla_decode_paged_planned_fp8(a["q"], a["cache"], a["s"], a["bt"], a["B"], a["n_q"], a["H"],
+                                                a["num_pages"], a["page"], a["maxp"], a["scale"], a["G"], a["ws"],
+                                                a["wsb"], a["err"], None)
+
+    for call in (dec, planned):
+        assert call(s=None) == 1
+        assert call(s=p + 4) == 1
+        assert call(cache=p + 1) == 1
+        assert call(scale=-1.0) == 1
+        assert call(n_q=3) == 2
+        assert call(page=128) == 2
+        assert call(wsb=ws - 1) == 3
+    assert dec(sl=None) == 1
