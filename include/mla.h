@@ -28,7 +28,10 @@
  *   - Tensors are dense, row-major, in the index order written beside each
  *     argument, and every pointer must be 16-byte aligned.
  *   - Supported shapes: d_nope = d_v = 128, d_r = 64, d_c = 512 (a cache row
- *     holds d_c + d_r = 576 values), page_size = 64, 1 <= H <= 128,
+ *     holds d_c + d_r = 576 values), page_size 64 or 128 tokens (Huny's
+ *     Dev Blog "MLA 아키텍처 해부" section 6 item 2: pages of 64-128 tokens;
+ *     the kernels read a page as one or two 64-token tiles), 1 <= H <= 128,
+ *     max_pages_per_seq * page_size <= 2^30,
  *     n_q in {1, 2}, 1 <= B <= MLA_MAX_BATCH. Other values return
  *     MLA_ERR_UNSUPPORTED_SHAPE without launching anything.
  *   - Argument errors found on the host return a status before any launch.
@@ -167,11 +170,14 @@ mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, cons
                                uint16_t* q_abs, int T, int H, int d_q, int d_r, int d_c, void* stream);
 
 /* ------------------------------------------------------------------------
- * Split-KV decode. The pages of all sequences, taken in sequence order, are
- * cut into G = min(num_splits, P) contiguous ranges of near-equal cost
- * (P = total pages). A worker (a pair of CTAs on two SMs) that moves on to
- * another sequence inside its range pays for the switch, so the pages are
- * laid on a cost line where sequence b (n_b pages, first global page P_b)
+ * Split-KV decode. The unit of work is a TILE of 64 tokens: a sequence of
+ * context L holds ceil(L / 64) tiles, tile t in page block_table[b][t * 64 /
+ * page_size] at row offset (t * 64) % page_size. The tiles of all sequences,
+ * taken in sequence order, are cut into G = min(num_splits, P) contiguous
+ * ranges of near-equal cost (P = total tiles; "page" below means tile). A
+ * worker (a pair of CTAs on two SMs) that moves on to another sequence inside
+ * its range pays for the switch, so the tiles are laid on a cost line where
+ * sequence b (n_b tiles, first global tile P_b)
  * occupies [P_b + a*b, P_b + a*b + n_b) behind a switch stretch of a = 3
  * points (for b >= 1); V = P + a*(B-1), and a = 0 instead when
  * floor((P + 3*(B-1)) / G) < 4. Cut p (0 < p < G) sits at x = floor(p*V/G)
@@ -193,12 +199,13 @@ mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, cons
  * Workspace layout (int32 unless noted; every block starts at a 256-byte
  * aligned offset; I = num_splits + B):
  *   hdr[64]                 hdr[0] = number of partials, hdr[1] = used splits,
- *                           hdr[2] = total pages
+ *                           hdr[2] = total tiles (P)
  *   range_item[num_splits+1] first partial index of each range
  *   seq_item[B+1]           first partial index of each sequence (partials of
  *                           sequence b are seq_item[b] .. seq_item[b+1]-1)
  *   seq_len_eff[B]          the context lengths actually used (clamped)
- *   item_seq[I], item_page0[I], item_page1[I]   sequence and page range
+ *   item_seq[I], item_tile0[I], item_tile1[I]   sequence and tile range
+ *                           [tile0, tile1) within the sequence
  *   lse_part[I][n_q][H]     float, natural-log sum-exp of the range's scores
  *   o_part[I][n_q][64][H][8] fp16, the range's softmax-normalised sum of
  *                           latents, head-minor in groups of eight columns:
@@ -215,7 +222,7 @@ size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);
  * For sequence b with context L = seq_lens[b] (which INCLUDES its n_q new
  * tokens), query j attends logical tokens s = 0 .. L - n_q + j, and
  *   z_s = softmax_scale * sum_{e < 576} q_abs[b][j][h][e] * row_s[e]
- *   row_s = cache[block_table[b][s / 64]][s % 64][0:576]
+ *   row_s = cache[block_table[b][s / page_size]][s % page_size][0:576]
  * (Huny's Dev Blog section 2.2: the cached row is c^KV (512) then the shared
  * rotated k^R (64); section 3.1: scoring in latent space; ikmyungterran.us
  * attention guide section 1.3: softmax(z / sqrt(d_k)); the pages give
@@ -280,7 +287,7 @@ mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache
  * mla_decode_paged_fp8 / mla_decode_paged_planned_fp8 — mla_decode_paged /
  * mla_decode_paged_planned on an FP8 cache: the same partials in the same
  * workspace (merged by mla_combine), computed on the dequantised latents
- *   row_s[d] = scales[d] * e4m3(cache8[block_table[b][s / 64]][s % 64][d]).
+ *   row_s[d] = scales[d] * e4m3(cache8[block_table[b][s / page_size]][s % page_size][d]).
  * Each code is read from HBM once. The scales are folded into the query (the
  * scores) and into the written partials (the values); the codes are widened to
  * fp16 in shared memory (exactly) and the MMAs take fp16 operands (the scaled
@@ -357,7 +364,7 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
  * pages (the step before decoding them):
  *   row[i] = sum_k h[t][k] w_dkr[i][k]         i < 576
  *   (row[512 + 2i], row[513 + 2i]) rotated by the angle pos * rope_theta^(-2i/64)
- *   cache[block_table[b][pos / 64]][pos % 64][0:576] = row (bf16, nearest even)
+ *   cache[block_table[b][pos / page_size]][pos % page_size][0:576] = row (bf16, nearest even)
  * for new row t = b * n_q + j at position pos = L - n_q + j, L = seq_lens[b]
  * (which already counts the new tokens). Huny's Dev Blog section 1.2: the
  * joint compression c_t^KV = h_t W^DKV; section 2.2: the decoupled positional
@@ -374,7 +381,7 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
  *               no initial contents needed. Calls sharing a workspace must
  *               not overlap on the GPU.
  * The sums over d_model are added in a fixed order, so results are
- * reproducible bit for bit. A context length outside [n_q, max_pages * 64]
+ * reproducible bit for bit. A context length outside [n_q, max_pages * page_size]
  * is clamped and a page id outside [0, num_pages) skips that row; both are
  * reported in err_word as MLA_ERR_BOUNDS. Starts after the kernel before it
  * on the stream has finished (h is usually that kernel's output). */

@@ -273,9 +273,10 @@ def out_comb(u, w_comb, out=None, *, workspace=None, stream=None):
 
 
 def decode_plan(seq_lens, *, n_q: int, H: int, max_pages: int, num_pages: int, num_splits: int | None = None,
-                workspace=None, err_word=None, stream=None):
+                workspace=None, err_word=None, stream=None, page_size: int = PAGE):
     """The split plan alone, into ``workspace`` (allocated if None). Returns (workspace,
-    num_splits); pass both to ``decode_paged(..., planned=True)``."""
+    num_splits); pass both to ``decode_paged(..., planned=True)``. ``page_size`` (64 or
+    128 tokens) must be the cache's."""
     import torch
     B = seq_lens.shape[0]
     if num_splits is None:
@@ -283,7 +284,7 @@ def decode_plan(seq_lens, *, n_q: int, H: int, max_pages: int, num_pages: int, n
     if workspace is None:
         workspace = torch.empty(workspace_bytes(B, n_q, H, num_splits), dtype=torch.uint8, device=seq_lens.device)
     assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
-    st = lib().mla_decode_plan(_ptr(seq_lens), B, n_q, H, num_pages, PAGE, max_pages, num_splits, _ptr(workspace),
+    st = lib().mla_decode_plan(_ptr(seq_lens), B, n_q, H, num_pages, page_size, max_pages, num_splits, _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _ptr(err_word), _stream(stream))
     _check(st, "mla_decode_plan")
     return workspace, num_splits
@@ -294,7 +295,8 @@ def decode_paged(q_abs, cache, block_table, seq_lens, *, n_q: int, num_splits: i
                  planned: bool = False):
     """Split-KV decode over the paged cache. Returns (workspace, num_splits).
 
-    q_abs [B*n_q, H, 576] (or [B, n_q, H, 576]), cache [num_pages, 64, 576],
+    q_abs [B*n_q, H, 576] (or [B, n_q, H, 576]), cache [num_pages, page_size, 576] with
+    page_size 64 or 128,
     block_table [B, max_pages] int32, seq_lens [B] int32 (contexts include the
     n_q new tokens). The workspace holds the plan and the partials for
     ``combine``.
@@ -464,7 +466,8 @@ def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q
     B, max_pages = block_table.shape
     T, H = q_nope.shape[0], q_nope.shape[1]
     ws, g = decode_plan(seq_lens, n_q=n_q, H=H, max_pages=max_pages, num_pages=cache.shape[0],
-                        num_splits=num_splits, workspace=bufs.get("workspace"), err_word=err_word, stream=stream)
+                        num_splits=num_splits, workspace=bufs.get("workspace"), err_word=err_word, stream=stream,
+                        page_size=cache.shape[1])
     q_abs = absorb_q(q_nope, q_rope, w_uk, bufs.get("q_abs"), stream)
     decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=g, softmax_scale=softmax_scale,
                  workspace=ws, err_word=err_word, stream=stream, planned=True)

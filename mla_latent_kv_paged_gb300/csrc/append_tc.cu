@@ -153,14 +153,16 @@ append_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_const
 __global__ void __launch_bounds__(kRow / 2)
 append_finalize_kernel(const float* __restrict__ partials, uint16_t* __restrict__ cache,
                        const int32_t* __restrict__ block_table, const int32_t* __restrict__ seq_lens, int T,
-                       int n_q, int num_pages, int max_pages, double theta, int NT, int S, int32_t* err_word) {
+                       int n_q, int num_pages, int page_size, int max_pages, double theta, int NT, int S,
+                       int32_t* err_word) {
   const int t = blockIdx.x, c = threadIdx.x, col = 2 * c;
   const int b = t / n_q, j = t % n_q;
   // independent of the partials: overlaps the GEMM kernel
   const int raw = seq_lens[b];
-  const int L = raw < n_q ? n_q : (raw > max_pages * kPage ? max_pages * kPage : raw);
+  const int max_tokens = max_pages * page_size;
+  const int L = raw < n_q ? n_q : (raw > max_tokens ? max_tokens : raw);
   const int pos = L - n_q + j;
-  const int page = block_table[(size_t)b * max_pages + pos / kPage];
+  const int page = block_table[(size_t)b * max_pages + pos / page_size];
   const double inv_freq = col >= kDC ? pow(theta, -2.0 * (double)((col - kDC) >> 1) / kDR) : 0.0;
   sm100::grid_dependency_wait();  // the partials come from the GEMM kernel
   sm100::grid_launch_dependents();
@@ -190,7 +192,7 @@ append_finalize_kernel(const float* __restrict__ partials, uint16_t* __restrict_
     if (c == 0) report_error(err_word, MLA_ERR_BOUNDS);
     return;
   }
-  reinterpret_cast<uint32_t*>(cache + ((size_t)page * kPage + pos % kPage) * kRow)[c] = pack_bf16x2(x, y);
+  reinterpret_cast<uint32_t*>(cache + ((size_t)page * page_size + pos % page_size) * kRow)[c] = pack_bf16x2(x, y);
 }
 
 template <int kNT>
@@ -210,8 +212,8 @@ cudaError_t launch_gemm(const CUtensorMap& mw, const CUtensorMap& mh, int d_mode
 size_t append_workspace_bytes(int T, int d_model) { return append_ws_bytes(T, d_model); }
 
 cudaError_t launch_append(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache, const int32_t* block_table,
-                          const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int max_pages,
-                          double theta, void* workspace, int32_t* err_word, cudaStream_t s) {
+                          const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int page_size,
+                          int max_pages, double theta, void* workspace, int32_t* err_word, cudaStream_t s) {
   const int T = B * n_q;
   const AppendShape a = append_shape(T, d_model);
   CUtensorMap mw, mh;
@@ -226,7 +228,7 @@ cudaError_t launch_append(const uint16_t* h, const uint16_t* w_dkr, uint16_t* ca
                                : launch_gemm<128>(mw, mh, d_model, partials, a, err_word, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(append_finalize_kernel, dim3(T), dim3(kRow / 2), 0, s, (const float*)partials, cache, block_table,
-                    seq_lens, T, n_q, num_pages, max_pages, theta, a.NT, a.S, err_word);
+                    seq_lens, T, n_q, num_pages, page_size, max_pages, theta, a.NT, a.S, err_word);
 }
 
 }  // namespace mla

@@ -173,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_kr,
                  const __grid_constant__ CUtensorMap map_qkr, const __grid_constant__ CUtensorMap map_q,
                  const int32_t* __restrict__ block_table, int n_q, int H, int max_pages, int num_pages,
-                 float sl2, Plan plan, const float* __restrict__ fp8_scales, int32_t* err_word) {
+                 int tile_shift, float sl2, Plan plan, const float* __restrict__ fp8_scales, int32_t* err_word) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -258,25 +258,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 #pragma unroll
     for (int i = 0; i < kStages; ++i) last_ph[i] = -1;
     bool ok = true;
-    // page cursors over (range, page): lanes hold 32 consecutive page ids
+    // tile cursors over (range, tile): lanes hold the page ids of 32 consecutive
+    // tiles (a page holds 1 << tile_shift tiles of 64 tokens)
+    const int tile_mask = (1 << tile_shift) - 1;
     struct Cursor {
       int it, pg, pg1, base, id_l;
       size_t row;  // block-table row of the current range
     };
     auto cur_load = [&](Cursor& c) {
       const int mine = c.base + lane;
-      c.id_l = mine < c.pg1 ? block_table[c.row + mine] : 0;
+      c.id_l = mine < c.pg1 ? block_table[c.row + (mine >> tile_shift)] : 0;
     };
     auto cur_init = [&](Cursor& c, int it) {
       c.it = it;
       if (it < it1) {
         c.row = (size_t)plan.item_seq[it] * max_pages;
-        c.pg = c.base = plan.item_page0[it];
-        c.pg1 = plan.item_page1[it];
+        c.pg = c.base = plan.item_tile0[it];
+        c.pg1 = plan.item_tile1[it];
         cur_load(c);
       }
     };
-    auto cur_next = [&](Cursor& c) -> int {  // page id at the cursor, then advance
+    auto cur_next = [&](Cursor& c) -> int {  // page id of the tile at the cursor, then advance
       const int id = __shfl_sync(0xffffffffu, c.id_l, c.pg - c.base);
       if (++c.pg == c.pg1) {
         cur_init(c, c.it + 1);
@@ -293,7 +295,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 #endif
     while (ok && ld.it < it1) {
       const int it = ld.it;
-      if (ld.pg == plan.item_page0[it]) {
+      if (ld.pg == plan.item_tile0[it]) {
         // first page of a range: the CTA's half of its query into the next two
         // ring slots (the score readers move it into tensor memory). Slot q holds
         // latent boxes [128 heads][64] for columns 256r + 128q + {0, 64} and, in
@@ -315,6 +317,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         }
         if (!ok) break;
       }
+      const int sub = ld.pg & tile_mask;  // the tile's place in its page
       const int pid = cur_next(ld);
       // an id outside the pool loads zeros (TMA bounds) and is reported
       if (lane == 0 && (pid < 0 || pid >= num_pages)) report_error(err_word, MLA_ERR_BOUNDS);
@@ -322,7 +325,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       if (lane == 0 && MLA_SMEM_OK(sbase + kOffStage + stage * kStageBytes, kStageBytes)) {
         const uint32_t fb = bar(FULL0 + stage);
         const uint32_t dst = sbase + kOffStage + stage * kStageBytes;
-        const int y = pid * kPage;
+        const int y = ((pid << tile_shift) + sub) * kTile;
         if (kF8) {
           // the codes into the upper half of the slot, unswizzled rows
           mbar_arrive_expect_tx(fb, kF8StageBytes);
@@ -380,7 +383,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         // ---- score MMAs: S = q_abs half . [c ; k^R] half of the page
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0;
-          const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+          const int ntiles = plan.item_tile1[it] - plan.item_tile0[it];
           // the range's query: the score readers have moved the latent half from
           // its two ring slots into tensor memory (and read the slots: free them);
           // the positional half stays in shared memory
@@ -413,7 +416,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         // tokens) and from shared memory (the peer's tokens)
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0;
-          const int ntiles = plan.item_page1[it] - plan.item_page0[it];
+          const int ntiles = plan.item_tile1[it] - plan.item_tile0[it];
           for (int q = 0; q < kQSlots; ++q)  // the range's query slots (released by the score issuer)
             if (++stage == kStages) { stage = 0; ph ^= 1u; }
           for (int i = 0; i < ntiles; ++i, ++g) {
@@ -528,8 +531,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
-        const int pg0 = plan.item_page0[it];
-        const int ntiles = plan.item_page1[it] - pg0;
+        const int pg0 = plan.item_tile0[it];
+        const int ntiles = plan.item_tile1[it] - pg0;
         const int n_att = plan.seq_len_eff[plan.item_seq[it]] - n_q + j + 1;  // tokens query j attends
         // the range's latent query half: this thread's head row from the two ring
         // slots (four [128][64] boxes, 128B-swizzled: 16-byte chunk c of row r at
@@ -604,7 +607,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           float v[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * sl2;
-          const int nvp = n_att - ((pg0 + i) * kPage + 32 * (int)peer);  // attended among the 32
+          const int nvp = n_att - ((pg0 + i) * kTile + 32 * (int)peer);  // attended among the 32
           float hi = -INFINITY, lo = INFINITY;
           if (nvp >= 32) {
 #pragma unroll
@@ -692,7 +695,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       };
       for (int it = it0; it < it1 && ok; ++it) {
         const int li = it - it0;
-        const int b = plan.item_seq[it], pg0 = plan.item_page0[it], pg1 = plan.item_page1[it];
+        const int b = plan.item_seq[it], pg0 = plan.item_tile0[it], pg1 = plan.item_tile1[it];
         const int L = plan.seq_len_eff[b];
         const int n_att = L - n_q + j + 1;
         const int ntiles = pg1 - pg0;
@@ -715,7 +718,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           }
           const int xb = g & 1;
           // this CTA's partial scores of its 32 tokens
-          const int nv = n_att - ((pg0 + i) * kPage + 32 * (int)rank);  // valid tokens among these 32
+          const int nv = n_att - ((pg0 + i) * kTile + 32 * (int)rank);  // valid tokens among these 32
           if (!wait_phase(bar(SF0 + xb), (g >> 1) & 1, abort_flag, err_word)) { ok = false; break; }
           tc_fence_after();
           {
@@ -760,15 +763,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
           // order and this group waited for page g-5 at page g-2.)
           const int pb = g % kPBufs;
           if (g >= kPBufs && !wait_phase(bar(PVD0 + pb), ((g / kPBufs) & 1) ^ 1, abort_flag, err_word)) { ok = false; break; }
-          const int rows_valid = L - (pg0 + i) * kPage;
-          if (rows_valid < kPage) {
+          const int rows_valid = L - (pg0 + i) * kTile;
+          if (rows_valid < kTile) {
             // slack rows past the context may hold any bits: zero this CTA's latent
             // half so 0-weight x NaN cannot reach O. The score MMAs have read the
             // stage (SF); the value MMAs read it after this group's P-ready arrive.
             const int stage = (g + kQSlots * (li + 1)) % kStages;  // ring slot of page g
             const uint32_t sa = sbase + kOffStage + stage * kStageBytes;
             (void)MLA_SMEM_OK(sa, 4 * kCBoxBytes);
-            const int nz = (kPage - rows_valid) * 4 * 8;  // 16-byte chunks
+            const int nz = (kTile - rows_valid) * 4 * 8;  // 16-byte chunks
             for (int z = gtid; z < nz; z += kGThreads) {
               const int rr = rows_valid + z / 32, cb = (z / 8) & 3, ch = z & 7;
               asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(sa + cb * kCBoxBytes + rr * 128 + ch * 16),
@@ -956,7 +959,8 @@ namespace {
 template <bool kF8>
 cudaError_t launch_decode_impl(const CUtensorMap& map_c, const CUtensorMap& map_kr, const uint16_t* q_abs,
                                const float* fp8_scales, const int32_t* block_table, int B, int n_q, int H,
-                               int num_pages, int max_pages, float scale, int G, const Plan& plan, int32_t* err_word,
+                               int num_pages, int page_size, int max_pages, float scale, int G, const Plan& plan,
+                               int32_t* err_word,
                                cudaStream_t s) {
   CUtensorMap map_qkr, map_q;
   const uint64_t q_dims[2] = {kRow, (uint64_t)B * n_q * H};
@@ -970,36 +974,38 @@ cudaError_t launch_decode_impl(const CUtensorMap& map_c, const CUtensorMap& map_
   const float sl2 = scale * 1.4426950408889634f;
   dim3 grid(2 * G, n_q, 1);
   return launch_pdl(decode_tc_kernel<kF8>, grid, dim3(kThreads), kSmemBytes, s, map_c, map_kr, map_qkr, map_q,
-                    block_table, n_q, H, max_pages, num_pages, sl2, plan, fp8_scales, err_word);
+                    block_table, n_q, H, max_pages, num_pages, page_size == 2 * kTile ? 1 : 0, sl2, plan,
+                    fp8_scales, err_word);
 }
 }  // namespace
 
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
-                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
+                          int B, int n_q, int H, int num_pages, int page_size, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s) {
   CUtensorMap map_c, map_kr;
-  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * page_size};
   const uint64_t row_stride[1] = {kRow * 2};
   const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64};
   if (!make_tmap(&map_c, cache, 2, cache_dims, row_stride, box_c, 128) ||
       !make_tmap(&map_kr, cache, 2, cache_dims, row_stride, box_kr, 64))
     return cudaErrorInvalidValue;
-  return launch_decode_impl<false>(map_c, map_kr, q_abs, nullptr, block_table, B, n_q, H, num_pages, max_pages,
-                                   scale, G, plan, err_word, s);
+  return launch_decode_impl<false>(map_c, map_kr, q_abs, nullptr, block_table, B, n_q, H, num_pages, page_size,
+                                   max_pages, scale, G, plan, err_word, s);
 }
 
 cudaError_t launch_decode_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* fp8_scales,
-                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int max_pages,
-                              float scale, int G, const Plan& plan, int32_t* err_word, cudaStream_t s) {
+                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int page_size,
+                              int max_pages, float scale, int G, const Plan& plan, int32_t* err_word,
+                              cudaStream_t s) {
   CUtensorMap map_c, map_kr;
-  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * kPage};
+  const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * page_size};
   const uint64_t row_stride[1] = {kRow};
   const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64};
   if (!make_tmap(&map_c, cache8, 2, cache_dims, row_stride, box_c, 0, true) ||
       !make_tmap(&map_kr, cache8, 2, cache_dims, row_stride, box_kr, 0, true))
     return cudaErrorInvalidValue;
-  return launch_decode_impl<true>(map_c, map_kr, q_abs, fp8_scales, block_table, B, n_q, H, num_pages, max_pages,
-                                  scale, G, plan, err_word, s);
+  return launch_decode_impl<true>(map_c, map_kr, q_abs, fp8_scales, block_table, B, n_q, H, num_pages, page_size,
+                                  max_pages, scale, G, plan, err_word, s);
 }
 
 }  // namespace mla

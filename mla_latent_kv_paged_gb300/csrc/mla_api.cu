@@ -139,10 +139,9 @@ mla_status decode_args(void* workspace, size_t workspace_bytes, int B, int n_q, 
                        int page_size, int max_pages_per_seq, int num_splits, Plan* plan) {
   if (!workspace || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   if (B < 1 || num_pages < 1 || max_pages_per_seq < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
-  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H) || page_size != kPage)
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H) || !page_size_ok(page_size))
     return MLA_ERR_UNSUPPORTED_SHAPE;
-  if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
-    return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (!token_counts_ok(num_pages, page_size, max_pages_per_seq)) return MLA_ERR_UNSUPPORTED_SHAPE;
   const size_t need = plan_layout(nullptr, B, n_q, H, num_splits, nullptr);
   if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
   plan_layout(workspace, B, n_q, H, num_splits, plan);
@@ -165,10 +164,10 @@ mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                               num_splits, &plan);
   if (st != MLA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
-                                 err_word, s));
+  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, page_size, num_pages, num_splits,
+                                 plan, err_word, s));
   if (st != MLA_OK) return st;
-  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages,
+  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, page_size,
                                      max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
 }
 
@@ -195,10 +194,10 @@ mla_status mla_decode_paged_fp8(const uint16_t* q_abs, const uint8_t* cache8, co
                               num_splits, &plan);
   if (st != MLA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
-                                 err_word, s));
+  st = launch_status(launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, page_size, num_pages, num_splits,
+                                 plan, err_word, s));
   if (st != MLA_OK) return st;
-  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages,
+  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages, page_size,
                                          max_pages_per_seq, softmax_scale, num_splits, plan, err_word, s));
 }
 
@@ -214,7 +213,7 @@ mla_status mla_decode_paged_planned_fp8(const uint16_t* q_abs, const uint8_t* ca
   mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
                               num_splits, &plan);
   if (st != MLA_OK) return st;
-  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages,
+  return launch_status(launch_decode_fp8(q_abs, cache8, scales, block_table, B, n_q, H, num_pages, page_size,
                                          max_pages_per_seq, softmax_scale, num_splits, plan, err_word,
                                          (cudaStream_t)stream));
 }
@@ -227,8 +226,8 @@ mla_status mla_decode_plan(const int32_t* seq_lens, int B, int n_q, int H, int n
   mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
                               num_splits, &plan);
   if (st != MLA_OK) return st;
-  return launch_status(launch_plan(seq_lens, nullptr, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
-                                   err_word, (cudaStream_t)stream));
+  return launch_status(launch_plan(seq_lens, nullptr, B, n_q, max_pages_per_seq, page_size, num_pages, num_splits,
+                                   plan, err_word, (cudaStream_t)stream));
 }
 
 mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
@@ -242,7 +241,7 @@ mla_status mla_decode_paged_planned(const uint16_t* q_abs, const uint16_t* cache
   mla_status st = decode_args(workspace, workspace_bytes, B, n_q, H, num_pages, page_size, max_pages_per_seq,
                               num_splits, &plan);
   if (st != MLA_OK) return st;
-  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, max_pages_per_seq,
+  return launch_status(launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, page_size, max_pages_per_seq,
                                      softmax_scale, num_splits, plan, err_word, (cudaStream_t)stream));
 }
 
@@ -282,12 +281,11 @@ mla_status mla_append_kv(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cac
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || num_pages < 1 || max_pages_per_seq < 1) return MLA_ERR_INVALID_ARG;
   if (!(rope_theta > 1.f) || rope_theta != rope_theta) return MLA_ERR_INVALID_ARG;
-  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || page_size != kPage) return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !page_size_ok(page_size)) return MLA_ERR_UNSUPPORTED_SHAPE;
   if (d_model < 64 || d_model % 64 != 0 || d_model > 65536) return MLA_ERR_UNSUPPORTED_SHAPE;
-  if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
-    return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (!token_counts_ok(num_pages, page_size, max_pages_per_seq)) return MLA_ERR_UNSUPPORTED_SHAPE;
   if (workspace_bytes < append_workspace_bytes(B * n_q, d_model)) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  return launch_status(launch_append(h, w_dkr, cache, block_table, seq_lens, B, n_q, d_model, num_pages,
+  return launch_status(launch_append(h, w_dkr, cache, block_table, seq_lens, B, n_q, d_model, num_pages, page_size,
                                      max_pages_per_seq, (double)rope_theta, workspace, err_word,
                                      (cudaStream_t)stream));
 }

@@ -18,7 +18,7 @@ constexpr int kDR = 64;
 constexpr int kDC = 512;
 constexpr int kDV = 128;
 constexpr int kRow = kDC + kDR;  // 576 values per cached token
-constexpr int kPage = 64;
+constexpr int kTile = 64;  // tokens per tile, the decode kernel's unit; a page holds 1 or 2 tiles
 constexpr int kMaxHeads = 128;
 
 // ---------------------------------------------------------------- workspace
@@ -29,8 +29,8 @@ struct Plan {
   int32_t* seq_item;     // [B + 1]
   int32_t* seq_len_eff;  // [B]
   int32_t* item_seq;     // [I]
-  int32_t* item_page0;   // [I]
-  int32_t* item_page1;   // [I]
+  int32_t* item_tile0;   // [I] first tile (64 tokens) of the piece within its sequence
+  int32_t* item_tile1;   // [I] end tile (exclusive)
   float* lse_part;       // [I][n_q][H]
   uint16_t* o_part;      // [I][n_q][64][H][8] fp16, head-minor
 };
@@ -62,8 +62,8 @@ __host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H,
     p->seq_item = reinterpret_cast<int32_t*>(c + o_si);
     p->seq_len_eff = reinterpret_cast<int32_t*>(c + o_sl);
     p->item_seq = reinterpret_cast<int32_t*>(c + o_is);
-    p->item_page0 = reinterpret_cast<int32_t*>(c + o_p0);
-    p->item_page1 = reinterpret_cast<int32_t*>(c + o_p1);
+    p->item_tile0 = reinterpret_cast<int32_t*>(c + o_p0);
+    p->item_tile1 = reinterpret_cast<int32_t*>(c + o_p1);
     p->lse_part = reinterpret_cast<float*>(c + o_lse);
     p->o_part = reinterpret_cast<uint16_t*>(c + o_o);
   }
@@ -137,17 +137,24 @@ cudaError_t smem_limit(size_t bytes) {
 // ---------------------------------------------------------------- launchers
 // overlap: start beside the kernel enqueued before (programmatic dependent
 // launch); it then reads seq_lens and writes the plan while that kernel runs.
+// page_size: 64 or 128 tokens (1 or 2 tiles per block-table entry)
+inline bool page_size_ok(int page_size) { return page_size == kTile || page_size == 2 * kTile; }
+// sizes in tokens that stay in int32 (positions, and rows of the cache)
+inline bool token_counts_ok(int num_pages, int page_size, int max_pages) {
+  return (int64_t)max_pages * page_size <= INT32_MAX / 2 && (int64_t)num_pages * page_size <= INT32_MAX;
+}
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
-                        int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
+                        int max_pages, int page_size, int num_pages, int G, const Plan& plan, int32_t* err_word,
                         cudaStream_t s, bool overlap = true);
 cudaError_t launch_decode(const uint16_t* q_abs, const uint16_t* cache, const int32_t* block_table,
-                          int B, int n_q, int H, int num_pages, int max_pages, float scale, int G,
+                          int B, int n_q, int H, int num_pages, int page_size, int max_pages, float scale, int G,
                           const Plan& plan, int32_t* err_word, cudaStream_t s);
 // The same decode over an FP8 cache: e4m3 codes [num_pages][64][576] and one
 // float scale per column (fp8_scales[576]).
 cudaError_t launch_decode_fp8(const uint16_t* q_abs, const uint8_t* cache8, const float* fp8_scales,
-                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int max_pages,
-                              float scale, int G, const Plan& plan, int32_t* err_word, cudaStream_t s);
+                              const int32_t* block_table, int B, int n_q, int H, int num_pages, int page_size,
+                              int max_pages, float scale, int G, const Plan& plan, int32_t* err_word,
+                              cudaStream_t s);
 // e4m3 codes of bf16 rows of 576 values with per-column scales
 cudaError_t launch_quantize_fp8(const uint16_t* rows, const float* scales, uint8_t* codes, int64_t n_rows,
                                 cudaStream_t s);
@@ -168,7 +175,7 @@ cudaError_t launch_absorb_latent(const uint16_t* c_q, const uint16_t* q_rope, co
                                  int T, int H, int d_q, cudaStream_t s);
 size_t append_workspace_bytes(int T, int d_model);
 cudaError_t launch_append(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache, const int32_t* block_table,
-                          const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int max_pages,
-                          double theta, void* workspace, int32_t* err_word, cudaStream_t s);
+                          const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int page_size,
+                          int max_pages, double theta, void* workspace, int32_t* err_word, cudaStream_t s);
 
 }  // namespace mla

@@ -113,10 +113,9 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache, cons
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || num_pages < 1 || max_pages_per_seq < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || softmax_scale != softmax_scale) return MLA_ERR_INVALID_ARG;
-  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || H < 1 || H > kMaxHeads || page_size != kPage)
+  if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || H < 1 || H > kMaxHeads || !page_size_ok(page_size))
     return MLA_ERR_UNSUPPORTED_SHAPE;
-  if ((int64_t)max_pages_per_seq * kPage > INT32_MAX / 2 || (int64_t)num_pages * kPage > INT32_MAX)
-    return MLA_ERR_UNSUPPORTED_SHAPE;
+  if (!token_counts_ok(num_pages, page_size, max_pages_per_seq)) return MLA_ERR_UNSUPPORTED_SHAPE;
   // the plan and partials of this call must fit the fixed array
   if (plan_layout(nullptr, B, n_q, H, num_splits, nullptr) > kNoAllocScratchBytes)
     return MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -130,10 +129,10 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache, cons
   cudaStream_t s = (cudaStream_t)stream;
   // the plan waits for the kernel before it: that may be the previous call's
   // merge, still reading the plan in the shared array
-  cudaError_t e = launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, num_pages, num_splits, plan,
-                              err_word, s, /*overlap=*/false);
+  cudaError_t e = launch_plan(seq_lens, block_table, B, n_q, max_pages_per_seq, page_size, num_pages, num_splits,
+                              plan, err_word, s, /*overlap=*/false);
   if (e == cudaSuccess)
-    e = launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, max_pages_per_seq, softmax_scale,
+    e = launch_decode(q_abs, cache, block_table, B, n_q, H, num_pages, page_size, max_pages_per_seq, softmax_scale,
                       num_splits, plan, err_word, s);
   if (e == cudaSuccess) e = launch_combine(plan, B, n_q, H, u, lse, s);
   if (e != cudaSuccess) {

@@ -1,16 +1,18 @@
-// Split-KV work plan: cuts the pages of all sequences (in sequence order) into
-// G contiguous ranges of near-equal cost and lists the (sequence, page range)
-// pieces each range covers. A range that moves on to another sequence pays
-// for the switch (the accumulator of the finished piece is written out and
-// the next query is loaded), so every sequence start after the first counts
-// as kSwitchPages extra pages: the cuts are equal steps along that longer
-// line, and a cut that falls inside a switch lands on the sequence start.
+// Split-KV work plan: cuts the 64-token tiles of all sequences (in sequence
+// order; a page of 64 tokens is one tile, a page of 128 two) into G contiguous
+// ranges of near-equal cost and lists the (sequence, tile range) pieces each
+// range covers. A range that moves on to another sequence pays for the switch
+// (the accumulator of the finished piece is written out and the next query is
+// loaded), so every sequence start after the first counts as kSwitchPages extra
+// tiles: the cuts are equal steps along that longer line, and a cut that falls
+// inside a switch lands on the sequence start.
 // Flash-decoding over a paged cache: the Huny's Dev Blog "MLA 아키텍처 해부"
 // section 4 table names FlashDecoding / PagedAttention as the decode
 // techniques; section 6 item 2 sets MLA pages at 64-128 tokens.
 //
 // One block of 256 threads. Integer work only; the output is a pure function
-// of (seq_lens, n_q, max_pages, G), so repeated calls give identical plans.
+// of (seq_lens, n_q, max_pages * page_size, G), so repeated calls give
+// identical plans.
 #include "mla_internal.cuh"
 #include "sm100.cuh"
 
@@ -70,7 +72,7 @@ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return div_nn(a + b
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table, int B,
-            int n_q, int max_pages, int num_pages, int G, Plan plan, int32_t* err_word) {
+            int n_q, int max_tokens, int num_pages, int G, Plan plan, int32_t* err_word) {
   extern __shared__ int smem_i[];
   int* s_pstart = smem_i;            // [B+1] exclusive page prefix
   int* s_istart = smem_i + (B + 1);  // [B+1] exclusive piece prefix
@@ -81,19 +83,19 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   // grid dependency wait, which covers this kernel's completion
   sm100::grid_launch_dependents();
 
-  // 1. clamp context lengths, count pages
+  // 1. clamp context lengths (to the block table's max_pages * page_size tokens), count tiles
   for (int b = tid; b < B; b += kPlanThreads) {
     int L = seq_lens[b];
     if (L < n_q) {
       report_error(err_word, MLA_ERR_BOUNDS);
       L = n_q;
     }
-    if (L > max_pages * kPage) {
+    if (L > max_tokens) {
       report_error(err_word, MLA_ERR_BOUNDS);
-      L = max_pages * kPage;
+      L = max_tokens;
     }
     plan.seq_len_eff[b] = L;
-    s_pstart[b] = (L + kPage - 1) / kPage;
+    s_pstart[b] = (L + kTile - 1) / kTile;
   }
   __syncthreads();
   const int total = block_exclusive_scan(s_pstart, B, warp_sums);
@@ -142,14 +144,14 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     for (int64_t p = lo; p <= hi; ++p) {
       const int64_t x = div_nn(p * V, Ge) - a * b;  // global page of the cut
       plan.item_seq[k] = b;
-      plan.item_page0[k] = (int)(start - Pb);
-      plan.item_page1[k] = (int)(x - Pb);
+      plan.item_tile0[k] = (int)(start - Pb);
+      plan.item_tile1[k] = (int)(x - Pb);
       ++k;
       start = x;
     }
     plan.item_seq[k] = b;
-    plan.item_page0[k] = (int)(start - Pb);
-    plan.item_page1[k] = (int)(Eb - Pb);
+    plan.item_tile0[k] = (int)(start - Pb);
+    plan.item_tile1[k] = (int)(Eb - Pb);
     plan.seq_item[b] = s_istart[b];
   }
   if (tid == 0) plan.seq_item[B] = s_items;
@@ -192,8 +194,9 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
-                        int max_pages, int num_pages, int G, const Plan& plan, int32_t* err_word,
+                        int max_pages, int page_size, int num_pages, int G, const Plan& plan, int32_t* err_word,
                         cudaStream_t s, bool overlap) {
+  const int max_tokens = max_pages * page_size;
   const size_t smem = (size_t)2 * (B + 1) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -201,10 +204,10 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int
     if (e != cudaSuccess) return e;
   }
   if (overlap)
-    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, block_table, B, n_q, max_pages,
+    return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, block_table, B, n_q, max_tokens,
                       num_pages, G, plan, err_word);
   // after the previous kernel has finished (its grid dependency wait then returns at once)
-  plan_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, block_table, B, n_q, max_pages, num_pages, G, plan, err_word);
+  plan_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, block_table, B, n_q, max_tokens, num_pages, G, plan, err_word);
   return cudaGetLastError();
 }
 

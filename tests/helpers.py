@@ -57,13 +57,15 @@ def device_inputs(inp, pg):
     )
 
 
-def plan_mirror(seq_lens, n_q, max_pages, G, page=64, switch_pages=3):
+def plan_mirror(seq_lens, n_q, max_pages, G, page=64, switch_pages=3, tile=64):
     """Python statement of the split plan documented in include/mla.h (integer work):
-    pages of all sequences in order, each sequence start after the first costing
-    `switch_pages` extra pages (dropped when a step is not longer than that);
-    cut p at floor(p * V / G') on that line, G' = min(G, P)."""
+    contexts clipped to the block table's max_pages * page tokens, cut into tiles of
+    64 tokens; the tiles of all sequences in order, each sequence start after the
+    first costing `switch_pages` extra tiles (dropped when a step is not longer than
+    that); cut p at floor(p * V / G') on that line, G' = min(G, P). The items'
+    bounds are tile indices."""
     lens = np.clip(np.asarray(seq_lens, dtype=np.int64), n_q, max_pages * page)
-    pages = (lens + page - 1) // page
+    pages = (lens + tile - 1) // tile
     starts = np.concatenate([[0], np.cumsum(pages)])
     P = int(starts[-1])
     B = len(lens)

@@ -167,7 +167,10 @@ def test_host_validation_plan_and_planned_decode(lib):
                                             None)
 
     assert plan(sl=None) == 1 and plan(sl=p + 4) == 1 and plan(ws=None) == 1 and plan(B=0) == 1
-    assert plan(G=0) == 1 and plan(n_q=3) == 2 and plan(page=128) == 2 and plan(H=129) == 2
+    assert plan(G=0) == 1 and plan(n_q=3) == 2 and plan(H=129) == 2
+    # pages of 64 or 128 tokens; positions up to max_pages * page_size must stay below 2^30
+    assert plan(page=256) == 2 and plan(page=96) == 2 and plan(page=0) == 2
+    assert plan(page=128, maxp=(1 << 23) + 1) == 2 and plan(page=64, maxp=(1 << 24) + 1) == 2
     assert plan(wsb=ws - 1) == 3
     assert dec(q=None) == 1 and dec(bt=p + 4) == 1 and dec(scale=0.0) == 1 and dec(ws=p + 8) == 1
     assert dec(n_q=0) == 2
@@ -196,7 +199,8 @@ def test_host_validation_append(lib):
     assert app(theta=float("nan")) == 1
     assert app(n_q=3) == 2
     assert app(d=96) == 2
-    assert app(page=128) == 2
+    assert app(page=256) == 2 and app(page=32) == 2
+    assert app(page=128, maxp=(1 << 23) + 1) == 2
     assert app(wsb=ws - 1) == 3
 
 
@@ -331,6 +335,6 @@ def test_host_validation_fp8(lib):
         assert call(cache=p + 1) == 1
         assert call(scale=-1.0) == 1
         assert call(n_q=3) == 2
-        assert call(page=128) == 2
+        assert call(page=256) == 2 and call(page=128, maxp=(1 << 23) + 1) == 2
         assert call(wsb=ws - 1) == 3
     assert dec(sl=None) == 1
