@@ -313,6 +313,21 @@ def run_ours(args):
         combine(S)
         out_proj(S)
 
+    # FP8 latent cache (e4m3 codes, per-column scales): the same pages quantised on
+    # the device, then the planned decode call on them (not part of the timed step)
+    fp8_scales = torch.from_numpy(mi.fp8_channel_scales(inp)).to(dev)
+
+    def fp8_setup():
+        for S in sets:
+            S["cache8"] = mla.quantize_fp8(S["cache"], fp8_scales)
+
+    def quantize8(S):
+        mla.quantize_fp8(S["cache"], fp8_scales, S["cache8"])
+
+    def decode8_planned(S):
+        mla.decode_paged_fp8(S["q_abs"], S["cache8"], fp8_scales, S["bt"], S["sl"], n_q=n_q, num_splits=G,
+                             workspace=S["workspace"], err_word=err, planned=True)
+
     # eager warm-up (checks the error word), then CUDA graphs of back-to-back
     # steps so the timed region measures device time, not host launches
     for k in range(args.warmup):
@@ -321,7 +336,12 @@ def run_ours(args):
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item())}")
     if args.profile_phase:  # one side call alone, eagerly (short profiling runs)
-        fn = {"absorb_q_latent": absorb_latent, "out_comb": out_comb, "append_kv": append}[args.profile_phase]
+        fn = {"absorb_q_latent": absorb_latent, "out_comb": out_comb, "append_kv": append,
+              "fp8_decode": decode8_planned}[args.profile_phase]
+        if args.profile_phase == "fp8_decode":
+            fp8_setup()
+            for k in range(NSETS):
+                plan(sets[k])
         for k in range(6):
             fn(sets[k % NSETS])
         torch.cuda.synchronize()
@@ -403,19 +423,8 @@ def run_ours(args):
     latent_us = per_call_us(absorb_latent)
     comb_us = per_call_us(out_comb)
 
-    # FP8 latent cache (e4m3 codes, per-column scales): the same pages quantised on the
-    # device, then the planned decode call on them, timed like the bf16 one
-    fp8_scales = torch.from_numpy(mi.fp8_channel_scales(inp)).to(dev)
-    for S in sets:
-        S["cache8"] = mla.quantize_fp8(S["cache"], fp8_scales)
-
-    def quantize8(S):
-        mla.quantize_fp8(S["cache"], fp8_scales, S["cache8"])
-
-    def decode8_planned(S):
-        mla.decode_paged_fp8(S["q_abs"], S["cache8"], fp8_scales, S["bt"], S["sl"], n_q=n_q, num_splits=G,
-                             workspace=S["workspace"], err_word=err, planned=True)
-
+    # the FP8 cache's planned decode call, timed like the bf16 one
+    fp8_setup()
     for k in range(NSETS):
         plan(sets[k])
     fp8_dec_us = per_call_us(decode8_planned)
@@ -472,6 +481,7 @@ def run_ours(args):
         e2e_times.append(time.perf_counter() - t0)
     e2e_total = max_over_ranks(sum(e2e_times), dist, dev)
     e2e_value = job_rate(ws_, T, args.steps, e2e_total)
+    e2e_parts = e2e_breakdown(captured, stream, flush, e2e_times)
 
     if rank == 0:
         hbm, tflops, src = peaks()
@@ -493,7 +503,9 @@ def run_ours(args):
                          "tflops_achieved": wb["decode_flops"] / (dec_us * 1e-6) / 1e12,
                          "tensor_peak_tflops": tflops,
                          "duration": f"per call, {R} calls back to back over {NSETS} rotating input sets"},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "breakdown_us": e2e_parts},
+            "decode_plus_combine": decode_combine_line(dec_us, phases["combine"], dec_bytes, inp, hbm),
             "append_kv": append_line(append_us, T, hbm),
             "absorb_q_latent": latent_line(latent_us, phases["absorb_q"], T, H, hbm),
             "out_comb": comb_line(comb_us, phases["out_proj"], T, H, hbm),
@@ -511,6 +523,48 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def e2e_breakdown(captured, stream, flush, e2e_times, reps=30):
+    """Where an end-to-end step's time goes (medians, microseconds): the host's wall time
+    for one replay of the host-I/O graph plus its synchronisation; the device time of that
+    graph (CUDA events on the stream around the replay: both copies and the step); each
+    packed copy alone (events around one copy of the same pinned buffers); and the rest of
+    the wall time (graph launch and the host's wake-up after the stream completes)."""
+    import torch
+    dev_t, h2d_t, d2h_t = [], [], []
+    for _ in range(reps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        captured.replay_host()
+        e1.record(stream)
+        stream.synchronize()
+        dev_t.append(1e3 * e0.elapsed_time(e1))
+    for dst, src, acc in ((captured._dev_in, captured._host_in, h2d_t), (captured._host_out, captured._dev_out, d2h_t)):
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            acc.append(1e3 * e0.elapsed_time(e1))
+    wall = 1e6 * float(np.median(e2e_times))
+    device = float(np.median(dev_t))
+    return {"wall": wall, "device_graph": device, "h2d_copy": float(np.median(h2d_t)),
+            "d2h_copy": float(np.median(d2h_t)), "host_launch_and_wait": wall - device}
+
+
+def decode_combine_line(dec_us, comb_us, dec_bytes, inp, hbm):
+    """The decode unit of the measurement plan: the split-KV decode kernel and the merge of
+    its partials, with the merge's output (u in bf16, lse in fp32) added to the bytes."""
+    T, H = inp.B * inp.n_q, inp.H
+    nbytes = dec_bytes + T * H * (mi.D_C * 2 + 4)
+    us = dec_us + comb_us
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"us": us, "alg_bytes": nbytes, "achieved_gbs": achieved, "peak_gbs": hbm, "frac": achieved / hbm,
+            "bound": "hbm"}
 
 
 def decode_alg(inp):
@@ -608,6 +662,7 @@ def fp8_line(us, quant_us, inp, hbm, tflops, src, bf16_us):
             "cache_bytes_bf16": wb["cache_bytes"], "alg_bytes_per_launch": nbytes,
             "alg_flops_per_launch": wb["decode_flops"],
             **roofline_bound(wb["decode_flops"], nbytes, us, hbm, tflops), "peak_source": src,
+            "traffic": stored_traffic("fp8"),
             "speedup_vs_bf16_decode": bf16_us / us, "quantize_us": quant_us,
             "duration": "per call, back to back over the rotating input sets"}
 
@@ -642,10 +697,11 @@ def comb_line(us, out_proj_us, T, H, hbm):
             "unmerged_weight_bytes": H * 128 * 512 * 2 + D_MODEL * H * 128 * 2, "out_proj_us": out_proj_us}
 
 
-TRAFFIC_PROFILES = {2: "decode_tc_v3_b32_l4096.md", 4: "decode_tc_long_b4_l131072.md"}
+TRAFFIC_PROFILES = {2: "decode_tc_b32_l4096.md", 4: "decode_tc_long_b4_l131072.md",
+                    5: "decode_tc_two_token_b64_l8192.md", "fp8": "decode_tc_fp8_b32_l4096.md"}
 
 
-def stored_traffic(workload: int = WORKLOAD_INDEX):
+def stored_traffic(workload=WORKLOAD_INDEX):
     """dram bytes per decode launch from the committed ncu summary of this workload, if the
     kernel is unchanged since (None otherwise)."""
     if workload not in TRAFFIC_PROFILES:
@@ -686,7 +742,8 @@ def main():
                          "5: 64 x 8192 with two query tokens)")
     ap.add_argument("--quick", action="store_true",
                     help="time the steps only (no phase times, end-to-end leg or CPU baseline): for profiling runs")
-    ap.add_argument("--profile-phase", choices=["absorb_q_latent", "out_comb", "append_kv"], default=None,
+    ap.add_argument("--profile-phase", choices=["absorb_q_latent", "out_comb", "append_kv", "fp8_decode"],
+                    default=None,
                     help="after the warm-up, run this call 6 times over the rotating sets and stop: for profiling runs")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -83,3 +83,17 @@ def test_roofline_bound_follows_the_ridge_point():
     assert two["bound"] == "tensor" and two["unit"] == "TFLOP/s"
     assert two["achieved"] == pytest.approx(1170.0) and two["frac"] == pytest.approx(1170.0 / tf)
     assert two["flop_per_byte"] == pytest.approx(468.0)
+
+
+def test_decode_plus_combine_counts_the_merge_output():
+    """The decode unit's bytes: the decode kernel's algorithmic bytes plus the merged u (bf16)
+    and lse (fp32) the combine writes; at 32 x 4096, 155,721,856 + 32*128*(1024+4)."""
+    import bench
+    import mla_inputs as mi
+    inp = mi.make_inputs(B=2, H=4, n_q=1, seq_lens=[5, 7], seed=1)
+    dec_bytes, _ = bench.decode_alg(inp)
+    line = bench.decode_combine_line(30.0, 5.0, dec_bytes, inp, hbm=1000.0)
+    assert line["alg_bytes"] == dec_bytes + 2 * 4 * (512 * 2 + 4)
+    assert abs(line["us"] - 35.0) < 1e-12
+    assert abs(line["frac"] - line["alg_bytes"] / 35e-6 / 1e9 / 1000.0) < 1e-12
+    assert 155_721_856 + 32 * 128 * 1028 == 159_932_544  # the 32 x 4096 decode unit
