@@ -11,16 +11,17 @@
 // Layout of the work. One worker = a cluster of two CTAs on two SMs; CTA r
 // owns the feature half r of every cache row: latent columns [256r, 256r+256)
 // and positional columns [512+32r, 512+32r+32). It TMA-loads only its half of
-// each 64-token page (36 KB), so every cached byte is read from HBM once. The
-// 128 heads share every page tile in shared memory (the reuse the absorbed
-// formulation creates).
+// each 64-token tile (36 KB; a page of 64 tokens is one tile, a page of 128
+// two), so every cached byte is read from HBM once. The 128 heads share every
+// tile in shared memory (the reuse the absorbed formulation creates).
 //
 // Scores need all 576 columns: each CTA computes a partial score
 // S_r[128 heads][64 tokens] (K = 288) with tcgen05 MMAs into tensor memory.
 // The softmax of a page is split by tokens: CTA r finishes tokens
 // [32r, 32r+32). It sends the partial scores of the other 32 tokens to the
-// peer (fp16 in log2 units, 8 KB, st.async into the peer's shared memory), adds the
-// peer's partial for its own tokens, and both CTAs exchange their page
+// peer (log2 units, as fp16 offsets from a per-head midpoint sent in fp32:
+// 8.5 KB, st.async into the peer's shared memory), adds the peer's partial for
+// its own tokens, and both CTAs exchange their page
 // maxima so they share one exact running maximum per head. Each CTA then
 // exponentiates its 32 tokens into P (bf16): its own half goes to tensor
 // memory (the A operand of its value MMAs), a copy to the peer's shared
@@ -29,11 +30,11 @@
 // value MMAs (P x C[64][256]).
 //
 // Tensor memory (512 columns x 128 lanes of 32 bits): O [0,256), S [256,320),
-// this CTA's P half for two pages [320,352), the CTA's positional query half
-// [352,368) and latent query half [384,512), the A operands of the score MMAs.
+// this CTA's P half for three pages [320,368), the CTA's positional query half
+// [368,384) and latent query half [384,512), the A operands of the score MMAs.
 // Shared memory: 5-slot ring (180 KB) of page halves and, at the start of each
 // range, the query half (TMA into two slots; the score readers move it into
-// tensor memory), the peer's partial scores (one 8 KB
+// tensor memory), the peer's partial scores (one 8.5 KB
 // buffer per softmax group), the peer's P half (3 x 8 KB), the exchange vectors.
 //
 // Warps: 0 = TMA producer, 1 = score-MMA issuer (and TMEM owner), 2 =
@@ -384,9 +385,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
         for (int it = it0; it < it1 && ok; ++it) {
           const int li = it - it0;
           const int ntiles = plan.item_tile1[it] - plan.item_tile0[it];
-          // the range's query: the score readers have moved the latent half from
-          // its two ring slots into tensor memory (and read the slots: free them);
-          // the positional half stays in shared memory
+          // the range's query: the score readers have moved the latent and
+          // positional halves from their two ring slots into tensor memory (and
+          // read the slots: free them)
           if (!wait_phase(bar(QCF), li & 1, abort_flag, err_word)) { ok = false; break; }
           for (int q = 0; q < kQSlots; ++q) {
             mbar_arrive(bar(EMPTY0 + stage));
