@@ -37,11 +37,12 @@
  *   - Argument errors found on the host return a status before any launch.
  *     A failed launch returns MLA_ERR_CUDA (cudaGetLastError is consumed).
  *   - Kernels start while the kernel enqueued before them on the stream is
- *     still finishing (programmatic dependent launch): mla_absorb_q and
- *     mla_out_proj load their weights (w_uk, w_uv) in that time, so weights
- *     must not be written by the kernel enqueued just before the call. Every
- *     other input is read after that kernel has finished, except seq_lens
- *     and the workspace of mla_decode_paged (see its ordering rule).
+ *     still finishing (programmatic dependent launch): mla_absorb_q,
+ *     mla_out_proj and mla_append_kv load their weights (w_uk, w_uv, w_dkr)
+ *     in that time, so weights must not be written by the kernel enqueued
+ *     just before the call. Every other input is read after that kernel has
+ *     finished, except seq_lens and the workspace of mla_decode_paged (see
+ *     its ordering rule).
  *   - Errors that only the device can see (a context length out of range, a
  *     page id outside [0, num_pages), a wait that timed out) are written as
  *     the first nonzero mla_status into *err_word (a device int32 the caller
@@ -383,8 +384,10 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
  * The sums over d_model are added in a fixed order, so results are
  * reproducible bit for bit. A context length outside [n_q, max_pages * page_size]
  * is clamped and a page id outside [0, num_pages) skips that row; both are
- * reported in err_word as MLA_ERR_BOUNDS. Starts after the kernel before it
- * on the stream has finished (h is usually that kernel's output). */
+ * reported in err_word as MLA_ERR_BOUNDS. w_dkr is read while the kernel
+ * before it on the stream is still finishing (see the conventions above); h,
+ * the cache, block_table and seq_lens only after it has finished (h is usually
+ * that kernel's output). */
 size_t mla_append_workspace_bytes(int T, int d_model);
 mla_status mla_append_kv(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache,
                          const int32_t* block_table, const int32_t* seq_lens, int B, int n_q,

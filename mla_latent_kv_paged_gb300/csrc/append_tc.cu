@@ -84,8 +84,11 @@ append_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_const
     fence_mbar_init();
     prefetch_tmap(&map_w);
     prefetch_tmap(&map_h);
-    // this CTA's weights into L2 while the previous kernel finishes (a hint)
-    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_2d(&map_w, kb * 64, m * 128);
+    // this CTA's weights into shared memory while the previous kernel finishes
+    // (weights are never its output); the hidden states follow after the wait
+    mbar_arrive_expect_tx(bar_ld, (uint32_t)nkb * (kABox + kNT * 128));
+    const uint64_t pol = policy_evict_first();
+    for (int k = 0; k < nkb; ++k) tma_load_2d(sbase + k * kABox, &map_w, bar_ld, (kb0 + k) * 64, m * 128, pol);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kNT);
@@ -102,11 +105,8 @@ append_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_const
   bool ok = true;
   if (threadIdx.x == 0) {
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(bar_ld, (uint32_t)nkb * (kABox + kBBox));
-    for (int k = 0; k < nkb; ++k) {
-      tma_load_2d(sbase + k * kABox, &map_w, bar_ld, (kb0 + k) * 64, m * 128, pol);
+    for (int k = 0; k < nkb; ++k)
       tma_load_2d(sbase + off_b + k * kBBox, &map_h, bar_ld, (kb0 + k) * 64, tile * kNT, pol);
-    }
     ok = wait_phase(bar_ld, 0, abort_flag, err_word);
     if (ok) {
       tc_fence_after();
@@ -167,12 +167,21 @@ append_finalize_kernel(const float* __restrict__ partials, uint16_t* __restrict_
   sm100::grid_dependency_wait();  // the partials come from the GEMM kernel
   sm100::grid_launch_dependents();
   const float2* p = reinterpret_cast<const float2*>(partials + ((size_t)(t / NT) * S * NT + t % NT) * kPartCols + col);
+  // the partials of up to 32 splits in flight at once (one L2 round trip for the
+  // usual split counts), added in split order
   float x = 0.f, y = 0.f;
-#pragma unroll 6
-  for (int s = 0; s < S; ++s) {
-    const float2 v = __ldcg(p + (size_t)s * NT * kPartCols / 2);
-    x += v.x;
-    y += v.y;
+  constexpr int kInFlight = 32;
+  for (int s0 = 0; s0 < S; s0 += kInFlight) {
+    float2 v[kInFlight];
+#pragma unroll
+    for (int k = 0; k < kInFlight; ++k)
+      if (s0 + k < S) v[k] = __ldcg(p + (size_t)(s0 + k) * NT * kPartCols / 2);
+#pragma unroll
+    for (int k = 0; k < kInFlight; ++k)
+      if (s0 + k < S) {
+        x += v[k].x;
+        y += v[k].y;
+      }
   }
   if (col >= kDC) {
     // the angle pos * theta^(-2i/64), reduced to [-pi, pi] in double (positions
