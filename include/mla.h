@@ -214,6 +214,11 @@ mla_status mla_absorb_q_latent(const uint16_t* c_q, const uint16_t* q_rope, cons
  *                           A normalised partial is a convex combination of
  *                           cached latents, so |value| <= max |c|; values beyond
  *                           the fp16 range (65504) are reported as MLA_ERR_RANGE.
+ *   range_desc[num_splits+1][4]  range p's first partial and that partial's
+ *                           sequence, first tile and end tile: {range_item[p],
+ *                           item_seq, item_tile0, item_tile1} of it, or
+ *                           {range_item[p], -1, 0, 0} when the range is empty
+ *                           (one 16-byte read for the decode kernel)
  */
 int mla_decode_default_splits(int n_q);
 size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);

@@ -263,7 +263,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     // tiles (a page holds 1 << tile_shift tiles of 64 tokens)
     const int tile_mask = (1 << tile_shift) - 1;
     struct Cursor {
-      int it, pg, pg1, base, id_l;
+      int it, pg, pg1, base, id_l, pg0, seq;  // pg0, seq: the piece's first tile and its sequence
       size_t row;  // block-table row of the current range
     };
     auto cur_load = [&](Cursor& c) {
@@ -273,8 +273,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     auto cur_init = [&](Cursor& c, int it) {
       c.it = it;
       if (it < it1) {
-        c.row = (size_t)plan.item_seq[it] * max_pages;
-        c.pg = c.base = plan.item_tile0[it];
+        c.seq = plan.item_seq[it];
+        c.row = (size_t)c.seq * max_pages;
+        c.pg = c.base = c.pg0 = plan.item_tile0[it];
         c.pg1 = plan.item_tile1[it];
         cur_load(c);
       }
@@ -290,18 +291,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
       return id;
     };
     Cursor ld;
-    cur_init(ld, it0);
+    {  // the range's first piece from its 16-byte description
+      const int4 d0 = plan.range_desc[worker];
+      ld.it = d0.x;
+      if (d0.x < it1) {
+        ld.seq = d0.y;
+        ld.row = (size_t)d0.y * max_pages;
+        ld.pg = ld.base = ld.pg0 = d0.z;
+        ld.pg1 = d0.w;
+        cur_load(ld);
+      }
+    }
 #if MLA_DEBUG_CHECKS
     if (*reinterpret_cast<volatile int*>(&g_dbg_skip_producer)) ld.it = it1;  // load nothing
 #endif
     while (ok && ld.it < it1) {
       const int it = ld.it;
-      if (ld.pg == plan.item_tile0[it]) {
+      if (ld.pg == ld.pg0) {
         // first page of a range: the CTA's half of its query into the next two
         // ring slots (the score readers move it into tensor memory). Slot q holds
         // latent boxes [128 heads][64] for columns 256r + 128q + {0, 64} and, in
         // its last 4 KB, positional rows [64q, 64q + 64) of columns 512 + 32r.
-        const int qrow = (plan.item_seq[it] * n_q + j) * H;
+        const int qrow = (ld.seq * n_q + j) * H;
         for (int q = 0; q < kQSlots && ok; ++q) {
           if (!wait_phase(bar(EMPTY0 + stage), ph ^ 1u, abort_flag, err_word)) { ok = false; break; }
           if (lane == 0 && MLA_SMEM_OK(sbase + kOffStage + stage * kStageBytes, kStageBytes)) {

@@ -33,6 +33,7 @@ struct Plan {
   int32_t* item_tile1;   // [I] end tile (exclusive)
   float* lse_part;       // [I][n_q][H]
   uint16_t* o_part;      // [I][n_q][64][H][8] fp16, head-minor
+  int4* range_desc;      // [G + 1] {first item, its sequence, its first tile, its end tile}
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -55,6 +56,7 @@ __host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H,
   size_t o_p1 = take(I * 4);
   size_t o_lse = take(I * n_q * H * 4);
   size_t o_o = take(I * n_q * H * (size_t)kDC * 2);
+  size_t o_rd = take((size_t)(G + 1) * 16);
   if (base && p) {
     char* c = reinterpret_cast<char*>(base);
     p->hdr = reinterpret_cast<int32_t*>(c + o_hdr);
@@ -66,6 +68,7 @@ __host__ __device__ inline size_t plan_layout(void* base, int B, int n_q, int H,
     p->item_tile1 = reinterpret_cast<int32_t*>(c + o_p1);
     p->lse_part = reinterpret_cast<float*>(c + o_lse);
     p->o_part = reinterpret_cast<uint16_t*>(c + o_o);
+    p->range_desc = reinterpret_cast<int4*>(c + o_rd);
   }
   return off;
 }

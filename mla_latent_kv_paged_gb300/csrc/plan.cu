@@ -155,8 +155,10 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
     plan.seq_item[b] = s_istart[b];
   }
   if (tid == 0) plan.seq_item[B] = s_items;
+  __syncthreads();  // the pieces are written: step 4 copies each range's first one
 
-  // 4. first piece of each range
+  // 4. first piece of each range, and its description (one 16-byte load for the
+  // decode kernel's producer instead of two dependent ones)
   for (int p = tid; p <= G; p += kPlanThreads) {
     int r;
     if (p == 0) {
@@ -182,6 +184,13 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
       }
     }
     plan.range_item[p] = r;
+    int4 d = make_int4(r, -1, 0, 0);
+    if (r < s_items) {
+      d.y = plan.item_seq[r];
+      d.z = plan.item_tile0[r];
+      d.w = plan.item_tile1[r];
+    }
+    plan.range_desc[p] = d;
   }
 
   // Page ids are checked by the decode kernel when it reads them. The plan

@@ -251,6 +251,15 @@ def test_plan_is_bit_exact(mla):
     assert np.array_equal(i32(offs[4], n), pl["items"][:, 0])
     assert np.array_equal(i32(offs[5], n), pl["items"][:, 1])
     assert np.array_equal(i32(offs[6], n), pl["items"][:, 2])
+    # the range descriptions at the end of the workspace: each range's first piece
+    off_lse = off  # after item_tile1: lse_part, o_part, then range_desc
+    off_o = (off_lse + I * inp.n_q * inp.H * 4 + 255) // 256 * 256
+    off_rd = (off_o + I * inp.n_q * inp.H * 512 * 2 + 255) // 256 * 256
+    desc = ws[off_rd:off_rd + 16 * (G + 1)].view(np.int32).reshape(G + 1, 4)
+    for p in range(G + 1):
+        r = int(pl["range_item"][p])
+        want = [r, -1, 0, 0] if r >= n else [r, *(int(x) for x in pl["items"][r])]
+        assert list(desc[p]) == want, (p, list(desc[p]), want)
 
 
 @pytest.mark.parametrize("splits", [None, 7000])
