@@ -320,7 +320,12 @@ mla_status mla_decode_paged_planned_fp8(const uint16_t* q_abs, const uint8_t* ca
  * weight 0.
  *   workspace  as filled by mla_decode_paged with the same B, n_q, H, num_splits
  *   u          [B][n_q][H][512] bf16 output (round-to-nearest-even)
- *   lse        [B][n_q][H] float output (natural log), may be NULL */
+ *   lse        [B][n_q][H] float output (natural log), may be NULL
+ * Ordering: the plan part of the workspace (seq_item) is read while the kernel
+ * before is still finishing, so that kernel must be the decode call that
+ * produced the partials (or anything after which the plan is complete); the
+ * partials are read after it has finished. The kernel after the merge may
+ * start at once (it reads u and lse only after its own dependency wait). */
 mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_splits,
                        uint16_t* u, float* lse, void* stream);
 

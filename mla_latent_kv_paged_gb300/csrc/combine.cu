@@ -22,13 +22,20 @@ constexpr int kKB = 4;         // partials whose loads are in flight together
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(Plan plan, int n_q, int H, uint16_t* __restrict__ u, float* __restrict__ lse_out) {
   __shared__ uint32_t tile[128][kCols / 2 + 1];  // bf16 pairs, padded row
-  sm100::grid_dependency_wait();  // the partials come from the decode kernel
+  // The next kernel (the up-projection) may start now and load its weights
+  // while the decode kernel's last CTAs and this merge run; it reads u only
+  // after its own dependency wait.
   sm100::grid_launch_dependents();
   const int h = threadIdx.x & 127, part = threadIdx.x >> 7;
   const int bj = blockIdx.x;  // b * n_q + j
   const int c0 = blockIdx.y * kCols + 16 * part;  // this thread's first column
   const int b = bj / n_q, j = bj % n_q;
+  // The plan's piece ranges were written by a kernel that had finished before
+  // the decode kernel (the kernel before this one) passed its own dependency
+  // wait, and that kernel lets this one start only after that wait: they can be
+  // read before this kernel's wait. The partials cannot.
   const int k0 = plan.seq_item[b], k1 = plan.seq_item[b + 1];
+  sm100::grid_dependency_wait();  // the partials come from the decode kernel
   auto lse_of = [&](int k) { return plan.lse_part[((size_t)k * n_q + j) * H + h]; };
   float acc[16];
 #pragma unroll
