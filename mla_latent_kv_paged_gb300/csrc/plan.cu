@@ -200,12 +200,131 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
   sm100::grid_dependency_wait();
 }
 
+// The same plan for at most 32 sequences by one warp: lane b holds sequence b,
+// prefix sums are warp scans and the search for the sequence a cut lands in
+// reads the other lanes by shuffles, so the plan needs no block barrier and no
+// shared memory; each range's description is formed from the same quantities
+// instead of being read back. The arithmetic and its order are those of
+// plan_kernel, so the two give identical plans.
+__device__ __forceinline__ int warp_exclusive_scan(int v, int lane, int* total) {
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  *total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
+__global__ void __launch_bounds__(32, 1)
+plan_small_kernel(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_tokens, int G, Plan plan,
+                  int32_t* err_word) {
+  const int lane = threadIdx.x;
+  sm100::grid_launch_dependents();
+  const bool live = lane < B;
+  int n_b = 0;  // tiles of sequence `lane`
+  if (live) {
+    int L = seq_lens[lane];
+    if (L < n_q) {
+      report_error(err_word, MLA_ERR_BOUNDS);
+      L = n_q;
+    }
+    if (L > max_tokens) {
+      report_error(err_word, MLA_ERR_BOUNDS);
+      L = max_tokens;
+    }
+    plan.seq_len_eff[lane] = L;
+    n_b = (L + kTile - 1) / kTile;
+  }
+  int total;
+  const int P_b = warp_exclusive_scan(n_b, lane, &total);
+  const int Ge = min(G, total);
+  const int64_t V0 = (int64_t)total + (int64_t)kSwitchPages * (B - 1);
+  const int64_t a = (div_nn(V0, Ge) >= kSwitchPages + 1) ? kSwitchPages : 0;
+  const int64_t V = (int64_t)total + a * (B - 1);
+  const int64_t Qb = P_b + a * lane, Eq = (int64_t)(P_b + n_b) + a * lane;
+  const int64_t lo_b = max(ceil_div64((Qb + 1) * Ge, V), (int64_t)1);
+  const int64_t hi_b = min(ceil_div64(Eq * Ge, V) - 1, (int64_t)Ge - 1);
+  int items;
+  const int I_b = warp_exclusive_scan(live ? 1 + (int)max((int64_t)0, hi_b - lo_b + 1) : 0, lane, &items);
+  if (lane == 0) {
+    plan.hdr[0] = items;
+    plan.hdr[1] = Ge;
+    plan.hdr[2] = total;
+    plan.seq_item[B] = items;
+  }
+  if (live) {
+    int k = I_b;
+    int64_t start = P_b;
+    for (int64_t p = lo_b; p <= hi_b; ++p) {
+      const int64_t x = div_nn(p * V, Ge) - a * lane;
+      plan.item_seq[k] = lane;
+      plan.item_tile0[k] = (int)(start - P_b);
+      plan.item_tile1[k] = (int)(x - P_b);
+      ++k;
+      start = x;
+    }
+    plan.item_seq[k] = lane;
+    plan.item_tile0[k] = (int)(start - P_b);
+    plan.item_tile1[k] = n_b;
+    plan.seq_item[lane] = I_b;
+  }
+  // the line position where sequence b's stretch starts (b >= 1)
+  const int64_t key = (int64_t)P_b + a * (lane - 1);
+  for (int p0 = 0; p0 <= G; p0 += 32) {
+    const int p = p0 + lane;
+    const int64_t x = (p > 0 && p < Ge) ? div_nn((int64_t)p * V, Ge) : 0;
+    int lo = 0, hi = B - 1;
+#pragma unroll
+    for (int step = 0; step < 6; ++step) {
+      const int mid = (lo + hi + 1) >> 1;
+      const int64_t km = __shfl_sync(0xffffffffu, key, mid & 31);
+      if (lo < hi) {
+        if (km <= x) lo = mid; else hi = mid - 1;
+      }
+    }
+    const int b = lo;
+    const int P = __shfl_sync(0xffffffffu, P_b, b), nb = __shfl_sync(0xffffffffu, n_b, b);
+    const int Ib = __shfl_sync(0xffffffffu, I_b, b);
+    const int64_t lob = __shfl_sync(0xffffffffu, lo_b, b), hib = __shfl_sync(0xffffffffu, hi_b, b);
+    if (p > G) continue;
+    int r;
+    int4 d;
+    if (p >= Ge) {
+      r = items;
+      d = make_int4(r, -1, 0, 0);
+    } else {
+      const int64_t Q = P + a * b;
+      if (p == 0 || x <= Q) {  // on the switch into b or on its first tile: b's first piece
+        r = Ib;
+        const int t1 = lob <= hib ? (int)(div_nn(lob * V, Ge) - a * b - P) : nb;
+        d = make_int4(r, b, 0, t1);
+      } else {  // the piece that starts at cut p inside b
+        r = Ib + (int)(p - lob + 1);
+        const int t0 = (int)(x - a * b - P);
+        const int t1 = p + 1 <= hib ? (int)(div_nn((int64_t)(p + 1) * V, Ge) - a * b - P) : nb;
+        d = make_int4(r, b, t0, t1);
+      }
+    }
+    plan.range_item[p] = r;
+    plan.range_desc[p] = d;
+  }
+  sm100::grid_dependency_wait();
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, int B, int n_q,
                         int max_pages, int page_size, int num_pages, int G, const Plan& plan, int32_t* err_word,
                         cudaStream_t s, bool overlap) {
   const int max_tokens = max_pages * page_size;
+  if (B <= 32) {
+    if (overlap)
+      return launch_pdl(plan_small_kernel, dim3(1), dim3(32), 0, s, seq_lens, B, n_q, max_tokens, G, plan, err_word);
+    plan_small_kernel<<<1, 32, 0, s>>>(seq_lens, B, n_q, max_tokens, G, plan, err_word);
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)2 * (B + 1) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

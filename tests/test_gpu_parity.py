@@ -442,3 +442,55 @@ def test_outputs_stay_inside_their_buffers(mla):
                            before[k].view(torch.uint8) if v.dtype != torch.int32 else before[k]), k
     r["err"] = 0
     compare_full(inp, r)
+
+
+def plan_arrays(ws, B, G):
+    """The plan part of a decode workspace (host bytes) as numpy arrays, at the documented offsets."""
+    I = G + B
+    offs, off = [], 0
+    for nbytes in [64 * 4, (G + 1) * 4, (B + 1) * 4, B * 4, I * 4, I * 4, I * 4]:
+        offs.append(off)
+        off = (off + nbytes + 255) // 256 * 256
+    return offs, off
+
+
+PLAN_CASES = [
+    # (seq_lens, n_q, splits): one warp plans up to 32 sequences, a block beyond
+    ([1], 1, 1), ([1], 1, 5), ([64, 65], 1, 1), ([64, 65], 1, 3), ([4096] * 32, 1, 76),
+    ([4096] * 32, 1, 64), ([1, 2, 3] * 10 + [700, 9000], 1, 76), ([63, 64, 65, 127, 128, 129] * 5, 2, 17),
+    (list(range(2, 66, 2)), 2, 200), ([300] * 33, 1, 76), ([5000, 1, 1, 1] * 10, 1, 7),
+]
+
+
+@pytest.mark.parametrize("lens,n_q,G", PLAN_CASES)
+def test_plan_kernels_match_the_mirror(mla, lens, n_q, G):
+    """Both plan kernels (a warp for at most 32 sequences, a block beyond) against the Python
+    statement of the plan, every array bit for bit, including the range descriptions."""
+    import torch
+    B = len(lens)
+    max_pages = max((L + 63) // 64 for L in lens)
+    ws, g = mla.decode_plan(to_dev_i32(np.array(lens, dtype=np.int32)), n_q=n_q, H=8, max_pages=max_pages,
+                            num_pages=B * max_pages, num_splits=G)
+    torch.cuda.synchronize()
+    host = ws.cpu().numpy()
+    offs, off_lse = plan_arrays(host, B, G)
+    I = G + B
+
+    def i32(o, n):
+        return host[o:o + 4 * n].view(np.int32)
+
+    pl = plan_mirror(lens, n_q, max_pages, G)
+    n = len(pl["items"])
+    assert list(i32(offs[0], 3)) == [n, pl["Ge"], pl["total"]]
+    assert np.array_equal(i32(offs[1], G + 1), pl["range_item"])
+    assert np.array_equal(i32(offs[2], B + 1), pl["seq_item"])
+    assert np.array_equal(i32(offs[3], B), np.clip(lens, n_q, None))
+    for k in range(3):
+        assert np.array_equal(i32(offs[4 + k], n), pl["items"][:, k])
+    off_o = (off_lse + I * n_q * 8 * 4 + 255) // 256 * 256
+    off_rd = (off_o + I * n_q * 8 * 512 * 2 + 255) // 256 * 256
+    desc = host[off_rd:off_rd + 16 * (G + 1)].view(np.int32).reshape(G + 1, 4)
+    for p in range(G + 1):
+        r = int(pl["range_item"][p])
+        want = [r, -1, 0, 0] if r >= n else [r, *(int(x) for x in pl["items"][r])]
+        assert list(desc[p]) == want, (p, list(desc[p]), want)
