@@ -201,11 +201,10 @@ plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ bl
 }
 
 // The same plan for at most 32 sequences by one warp: lane b holds sequence b,
-// prefix sums are warp scans and the search for the sequence a cut lands in
-// reads the other lanes by shuffles, so the plan needs no block barrier and no
-// shared memory; each range's description is formed from the same quantities
-// instead of being read back. The arithmetic and its order are those of
-// plan_kernel, so the two give identical plans.
+// prefix sums are warp scans, and the lane of sequence b also writes the
+// ranges whose cut falls in b's part of the cost line (no search), so the plan
+// needs no block barrier and no shared memory. The cut positions and their
+// arithmetic are those of plan_kernel, so the two give identical plans.
 __device__ __forceinline__ int warp_exclusive_scan(int v, int lane, int* total) {
   int x = v;
 #pragma unroll
@@ -255,6 +254,15 @@ plan_small_kernel(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_
     plan.seq_item[B] = items;
   }
   if (live) {
+    // the pieces of sequence b, and the ranges whose cut falls in b's part of the
+    // cost line [Q_b - a, Eq_b) (from 0 for b = 0): a cut on the switch stretch,
+    // x <= Q_b, starts its range at b's first piece, a cut inside b at its own
+    const int64_t t1_first = lo_b <= hi_b ? div_nn(lo_b * V, Ge) - a * lane - P_b : n_b;
+    const int64_t p_first = lane == 0 ? 0 : ceil_div64((Qb - a) * Ge, V);
+    for (int64_t p = p_first; p < min(lo_b, (int64_t)Ge); ++p) {
+      plan.range_item[p] = I_b;
+      plan.range_desc[p] = make_int4(I_b, lane, 0, (int)t1_first);
+    }
     int k = I_b;
     int64_t start = P_b;
     for (int64_t p = lo_b; p <= hi_b; ++p) {
@@ -264,51 +272,19 @@ plan_small_kernel(const int32_t* __restrict__ seq_lens, int B, int n_q, int max_
       plan.item_tile1[k] = (int)(x - P_b);
       ++k;
       start = x;
+      const int64_t x1 = p + 1 <= hi_b ? div_nn((p + 1) * V, Ge) - a * lane : P_b + n_b;
+      plan.range_item[p] = k;
+      plan.range_desc[p] = make_int4(k, lane, (int)(x - P_b), (int)(x1 - P_b));
     }
     plan.item_seq[k] = lane;
     plan.item_tile0[k] = (int)(start - P_b);
     plan.item_tile1[k] = n_b;
     plan.seq_item[lane] = I_b;
   }
-  // the line position where sequence b's stretch starts (b >= 1)
-  const int64_t key = (int64_t)P_b + a * (lane - 1);
-  for (int p0 = 0; p0 <= G; p0 += 32) {
-    const int p = p0 + lane;
-    const int64_t x = (p > 0 && p < Ge) ? div_nn((int64_t)p * V, Ge) : 0;
-    int lo = 0, hi = B - 1;
-#pragma unroll
-    for (int step = 0; step < 6; ++step) {
-      const int mid = (lo + hi + 1) >> 1;
-      const int64_t km = __shfl_sync(0xffffffffu, key, mid & 31);
-      if (lo < hi) {
-        if (km <= x) lo = mid; else hi = mid - 1;
-      }
-    }
-    const int b = lo;
-    const int P = __shfl_sync(0xffffffffu, P_b, b), nb = __shfl_sync(0xffffffffu, n_b, b);
-    const int Ib = __shfl_sync(0xffffffffu, I_b, b);
-    const int64_t lob = __shfl_sync(0xffffffffu, lo_b, b), hib = __shfl_sync(0xffffffffu, hi_b, b);
-    if (p > G) continue;
-    int r;
-    int4 d;
-    if (p >= Ge) {
-      r = items;
-      d = make_int4(r, -1, 0, 0);
-    } else {
-      const int64_t Q = P + a * b;
-      if (p == 0 || x <= Q) {  // on the switch into b or on its first tile: b's first piece
-        r = Ib;
-        const int t1 = lob <= hib ? (int)(div_nn(lob * V, Ge) - a * b - P) : nb;
-        d = make_int4(r, b, 0, t1);
-      } else {  // the piece that starts at cut p inside b
-        r = Ib + (int)(p - lob + 1);
-        const int t0 = (int)(x - a * b - P);
-        const int t1 = p + 1 <= hib ? (int)(div_nn((int64_t)(p + 1) * V, Ge) - a * b - P) : nb;
-        d = make_int4(r, b, t0, t1);
-      }
-    }
-    plan.range_item[p] = r;
-    plan.range_desc[p] = d;
+  // ranges past the last cut are empty
+  for (int p = Ge + lane; p <= G; p += 32) {
+    plan.range_item[p] = items;
+    plan.range_desc[p] = make_int4(items, -1, 0, 0);
   }
   sm100::grid_dependency_wait();
 }
