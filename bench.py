@@ -529,7 +529,7 @@ def e2e_breakdown(captured, stream, flush, e2e_times, reps=30):
     """Where an end-to-end step's time goes (medians, microseconds): the host's wall time
     for one replay of the host-I/O graph plus its synchronisation; the device time of that
     graph (CUDA events on the stream around the replay: both copies and the step); each
-    packed copy alone (events around one copy of the same pinned buffers); and the rest of
+    packed copy alone (events around one mla_copy16 of the same pinned buffers); and the rest of
     the wall time (graph launch and the host's wake-up after the stream completes)."""
     import torch
     dev_t, h2d_t, d2h_t = [], [], []
@@ -542,11 +542,12 @@ def e2e_breakdown(captured, stream, flush, e2e_times, reps=30):
         e1.record(stream)
         stream.synchronize()
         dev_t.append(1e3 * e0.elapsed_time(e1))
+    import mla_latent_kv_paged_gb300 as mla
     for dst, src, acc in ((captured._dev_in, captured._host_in, h2d_t), (captured._host_out, captured._dev_out, d2h_t)):
-        for _ in range(reps):
+        for _ in range(reps):  # the graph's own copies: mla_copy16 kernels on the pinned buffers
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            dst.copy_(src, non_blocking=True)
+            mla.copy16(src, dst, stream)
             e1.record(stream)
             stream.synchronize()
             acc.append(1e3 * e0.elapsed_time(e1))

@@ -405,6 +405,21 @@ mla_status mla_append_kv(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cac
                          float rope_theta, void* workspace, size_t workspace_bytes,
                          int32_t* err_word, void* stream);
 
+/* ------------------------------------------------------------------------
+ * mla_copy16 — bytes copied from src to dst by a kernel on `stream`, for the
+ * host I/O of a serving step: each of src and dst is device memory or pinned
+ * (page-locked, mapped) host memory, which a GB300 kernel reads and writes
+ * over NVLink-C2C; with every SM's accesses in flight a copy of a megabyte or
+ * two takes a fraction of a copy-engine transfer's fixed cost.
+ *   src, dst   16-byte aligned, not overlapping
+ *   bytes      a positive multiple of 16
+ * Pageable host memory, or a pointer the CUDA runtime does not know, returns
+ * MLA_ERR_INVALID_ARG before any launch (checked with cudaPointerGetAttributes).
+ * Unlike the decode calls this is an ordinary launch: it starts after the
+ * kernel before it on the stream has finished, and the kernel after it starts
+ * after it has finished. */
+mla_status mla_copy16(const void* src, void* dst, size_t bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

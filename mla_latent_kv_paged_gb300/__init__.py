@@ -47,6 +47,7 @@ EXPORTS = [
     "mla_merge_w_kq", "mla_absorb_q_latent",
     "mla_merge_w_comb", "mla_out_comb_workspace_bytes", "mla_out_comb",
     "mla_quantize_fp8", "mla_decode_paged_fp8", "mla_decode_paged_planned_fp8",
+    "mla_copy16",
 ]
 
 
@@ -145,6 +146,8 @@ def _load(path: str):
     L.mla_out_comb.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
     L.mla_quantize_fp8.restype = i
     L.mla_quantize_fp8.argtypes = [vp, vp, vp, ctypes.c_int64, vp]
+    L.mla_copy16.restype = i
+    L.mla_copy16.argtypes = [vp, vp, sz, vp]
     L.mla_decode_paged_fp8.restype = i
     L.mla_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp, vp]
     L.mla_decode_paged_planned_fp8.restype = i
@@ -342,6 +345,16 @@ def combine(workspace, *, B: int, n_q: int, H: int, num_splits: int, u=None, lse
     return u, lse
 
 
+def copy16(src, dst, stream=None):
+    """Copy the bytes of tensor ``src`` into ``dst`` (same byte size, a multiple of 16,
+    contiguous) with a kernel: device tensors or pinned host tensors, in any combination."""
+    assert src.is_contiguous() and dst.is_contiguous(), "tensors must be contiguous"
+    nbytes = src.numel() * src.element_size()
+    assert nbytes == dst.numel() * dst.element_size(), "byte sizes differ"
+    _check(lib().mla_copy16(_ptr(src), _ptr(dst), nbytes, _stream(stream)), "mla_copy16")
+    return dst
+
+
 def quantize_fp8(rows, scales, codes=None, stream=None):
     """e4m3 codes of bf16 rows [..., 576] with per-column scales [576] float32 (FP8 latent cache)."""
     import torch
@@ -495,7 +508,8 @@ class CapturedStep:
     q_nope, q_rope, block_table, seq_lens in; out, lse out), packed into one
     input and one output area, and a second graph that copies the inputs to
     the device in one copy, runs the step on them and copies out and lse back
-    in one copy. One serving step is then: write the new inputs into
+    in one copy (both copies are kernels that read or write the pinned memory,
+    ``copy16``). One serving step is then: write the new inputs into
     ``.host``, call ``replay_host()``, synchronise the stream, read
     ``.host["out"]``. (That graph uses the block table and lengths of
     ``.host``, not the block_table / seq_lens tensors given here.)
@@ -561,10 +575,12 @@ class CapturedStep:
             io_args = (d_in["q_nope"], d_in["q_rope"], w_uk, w_uv, cache, d_in["block_table"], d_in["seq_lens"])
             io_kw = dict(kw, bufs=io_bufs)
 
+            # the packed copies run as kernels of the library (mla_copy16): the GPU
+            # reads and writes the pinned buffers itself
             def io_step():
-                self._dev_in.copy_(self._host_in, non_blocking=True)
+                copy16(self._host_in, self._dev_in)
                 decode_step(*io_args, **io_kw)
-                self._host_out.copy_(self._dev_out, non_blocking=True)
+                copy16(self._dev_out, self._host_out)
 
             self.graph_io = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.graph_io):

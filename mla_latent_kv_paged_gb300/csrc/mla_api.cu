@@ -21,6 +21,28 @@ mla_status launch_status(cudaError_t e) {
 
 bool heads_ok(int H) { return H >= 1 && H <= kMaxHeads; }
 
+// The address a kernel uses for p: device or managed memory as it is, pinned
+// host memory through its mapped device address; false for memory the device
+// cannot address (pageable host memory) or when the runtime cannot tell.
+bool device_address(const void* p, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return true;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    // the same offset inside the allocation
+    *out = static_cast<const char*>(a.devicePointer) +
+           (static_cast<const char*>(p) - static_cast<const char*>(a.hostPointer));
+    return true;
+  }
+  return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -264,6 +286,15 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, 
   if (T < 1) return MLA_ERR_INVALID_ARG;
   if (d_c != kDC || d_v != kDV || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
   return launch_status(launch_out_proj(u, w_uv, out, T, H, (cudaStream_t)stream));
+}
+
+mla_status mla_copy16(const void* src, void* dst, size_t bytes, void* stream) {
+  if (!src || !dst || bytes == 0 || bytes % 16 != 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return MLA_ERR_INVALID_ARG;
+  const void* s_dev = nullptr;
+  const void* d_dev = nullptr;
+  if (!device_address(src, &s_dev) || !device_address(dst, &d_dev)) return MLA_ERR_INVALID_ARG;
+  return launch_status(launch_copy16(s_dev, const_cast<void*>(d_dev), bytes, (cudaStream_t)stream));
 }
 
 size_t mla_append_workspace_bytes(int T, int d_model) {

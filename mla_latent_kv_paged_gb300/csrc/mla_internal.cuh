@@ -177,6 +177,9 @@ cudaError_t launch_out_comb(const uint16_t* u, const uint16_t* w_comb, uint16_t*
 cudaError_t launch_absorb_latent(const uint16_t* c_q, const uint16_t* q_rope, const uint16_t* w_kq, uint16_t* q_abs,
                                  int T, int H, int d_q, cudaStream_t s);
 size_t append_workspace_bytes(int T, int d_model);
+// bytes (a multiple of 16) from src to dst, both device addresses (device
+// memory, or pinned host memory through its device address)
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_append(const uint16_t* h, const uint16_t* w_dkr, uint16_t* cache, const int32_t* block_table,
                           const int32_t* seq_lens, int B, int n_q, int d_model, int num_pages, int page_size,
                           int max_pages, double theta, void* workspace, int32_t* err_word, cudaStream_t s);

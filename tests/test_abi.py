@@ -338,3 +338,13 @@ def test_host_validation_fp8(lib):
         assert call(page=256) == 2 and call(page=128, maxp=(1 << 23) + 1) == 2
         assert call(wsb=ws - 1) == 3
     assert dec(sl=None) == 1
+
+
+def test_host_validation_copy16(lib):
+    p = FAKE
+    assert lib.mla_copy16(None, p, 16, None) == 1
+    assert lib.mla_copy16(p, None, 16, None) == 1
+    assert lib.mla_copy16(p, p + 16, 0, None) == 1
+    assert lib.mla_copy16(p, p + 64, 24, None) == 1       # not a multiple of 16
+    assert lib.mla_copy16(p + 8, p + 64, 16, None) == 1   # misaligned
+    assert lib.mla_copy16(p, p + 64, 16, None) == 1       # an address the runtime does not know
