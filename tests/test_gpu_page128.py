@@ -165,3 +165,17 @@ def test_append_writes_row_pos_mod_128(mla):
     for b, p in enumerate(pos):
         mask[pg.block_table[b][p // 128], p % 128] = False
     assert np.array_equal(after[mask], before[mask])
+
+
+def test_maximum_batch_in_pages_of_128(mla):
+    """4096 short contexts in pages of 128 (the block plan kernel, tiles at both offsets of a
+    page), and splits beyond the number of tiles (empty ranges)."""
+    lens = np.random.default_rng(128).integers(1, 260, size=4096)
+    lens[:4] = [1, 64, 65, 129]
+    inp = mi.make_inputs(B=4096, H=8, n_q=1, seq_lens=list(lens), seed=128)
+    pg = mi.make_paged(inp, spare_pages=2, page=128)
+    for splits in (None, 9000):
+        r = run_step(mla, inp, pg, num_splits=splits)
+        assert r["err"] == 0
+        compare_full(inp, r)
+

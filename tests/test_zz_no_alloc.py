@@ -100,3 +100,25 @@ def test_noalloc_back_to_back_calls_with_different_lengths():
     for i, (u, lse) in outs:
         assert np.array_equal(dev_to_bits(u), dev_to_bits(refs[i][0]))
         assert np.array_equal(lse.cpu().numpy().view(np.uint32), refs[i][1].cpu().numpy().view(np.uint32))
+
+
+def test_noalloc_in_pages_of_128():
+    import torch
+
+    import mla_latent_kv_paged_gb300 as mla
+    mla.build()
+    inp = mi.make_inputs(B=4, H=128, n_q=2, seq_lens=[3, 127, 129, 700], seed=171)
+    pg = mi.make_paged(inp, spare_pages=2, page=128)
+    d = device_inputs(inp, pg)
+    q_abs = mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"])
+    T, H = inp.B * inp.n_q, inp.H
+    u = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.decode_noalloc(q_abs, d["cache"], d["block_table"], d["seq_lens"], n_q=inp.n_q, num_splits=5, u=u,
+                       lse=lse, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.absorbed_f64(inp)
+    assert_close(dev_bf16_to_f64(u).reshape(T * H, 512), ref["u"], "u")
+    assert_close(lse.double().cpu().numpy().reshape(T * H), ref["lse"], "lse")
