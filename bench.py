@@ -481,7 +481,7 @@ def run_ours(args):
         e2e_times.append(time.perf_counter() - t0)
     e2e_total = max_over_ranks(sum(e2e_times), dist, dev)
     e2e_value = job_rate(ws_, T, args.steps, e2e_total)
-    e2e_parts = e2e_breakdown(captured, stream, flush, e2e_times)
+    e2e_parts = e2e_breakdown(captured, S0["w_uv"], stream, flush, e2e_times)
 
     if rank == 0:
         hbm, tflops, src = peaks()
@@ -525,36 +525,39 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def e2e_breakdown(captured, stream, flush, e2e_times, reps=30):
+def e2e_breakdown(captured, w_uv, stream, flush, e2e_times, reps=30):
     """Where an end-to-end step's time goes (medians, microseconds): the host's wall time
     for one replay of the host-I/O graph plus its synchronisation; the device time of that
-    graph (CUDA events on the stream around the replay: both copies and the step); each
-    packed copy alone (events around one mla_copy16 of the same pinned buffers); and the rest of
-    the wall time (graph launch and the host's wake-up after the stream completes)."""
+    graph (CUDA events on the stream around the replay: the input copy and the step, whose
+    out_proj and combine write out and lse into pinned host memory); the packed input copy
+    alone (events around one mla_copy16 of the same pinned buffers); out_proj alone writing
+    its output into the pinned host buffer and into device memory (the difference is what
+    the output's trip over the host link adds); and the rest of the wall time (graph launch
+    and the host's wake-up after the stream completes)."""
     import torch
-    dev_t, h2d_t, d2h_t = [], [], []
-    for _ in range(reps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        captured.replay_host()
-        e1.record(stream)
-        stream.synchronize()
-        dev_t.append(1e3 * e0.elapsed_time(e1))
     import mla_latent_kv_paged_gb300 as mla
-    for dst, src, acc in ((captured._dev_in, captured._host_in, h2d_t), (captured._host_out, captured._dev_out, d2h_t)):
-        for _ in range(reps):  # the graph's own copies: mla_copy16 kernels on the pinned buffers
+
+    def timed(fn):
+        acc = []
+        for _ in range(reps):
+            flush.zero_()
+            torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            mla.copy16(src, dst, stream)
+            fn()
             e1.record(stream)
             stream.synchronize()
             acc.append(1e3 * e0.elapsed_time(e1))
+        return float(np.median(acc))
+
+    device = timed(captured.replay_host)
+    h2d = timed(lambda: mla.copy16(captured._host_in, captured._dev_in, stream))
+    u = captured.bufs["u"]
+    out_host = timed(lambda: mla.out_proj(u, w_uv, captured.host["out"], stream))
+    out_dev = timed(lambda: mla.out_proj(u, w_uv, captured.bufs["out"], stream))
     wall = 1e6 * float(np.median(e2e_times))
-    device = float(np.median(dev_t))
-    return {"wall": wall, "device_graph": device, "h2d_copy": float(np.median(h2d_t)),
-            "d2h_copy": float(np.median(d2h_t)), "host_launch_and_wait": wall - device}
+    return {"wall": wall, "device_graph": device, "h2d_copy": h2d, "out_proj_to_host": out_host,
+            "out_proj_to_device": out_dev, "host_launch_and_wait": wall - device}
 
 
 def decode_combine_line(dec_us, comb_us, dec_bytes, inp, hbm):

@@ -20,8 +20,9 @@
  * -> mla_combine -> mla_out_proj).
  *
  * Conventions shared by every call:
- *   - All tensor pointers are DEVICE pointers, owned and allocated by the
- *     caller; the library never allocates, frees or synchronises. Every call
+ *   - All tensor pointers are DEVICE pointers (except where a call says that
+ *     pinned host memory is accepted), owned and allocated by the caller; the
+ *     library never allocates, frees or synchronises. Every call
  *     only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and returns.
  *   - bf16 tensors are passed as uint16_t* holding IEEE bfloat16 bit patterns.
@@ -320,7 +321,12 @@ mla_status mla_decode_paged_planned_fp8(const uint16_t* q_abs, const uint8_t* ca
  * weight 0.
  *   workspace  as filled by mla_decode_paged with the same B, n_q, H, num_splits
  *   u          [B][n_q][H][512] bf16 output (round-to-nearest-even)
- *   lse        [B][n_q][H] float output (natural log), may be NULL
+ *   lse        [B][n_q][H] float output (natural log), may be NULL; device
+ *              memory or pinned (page-locked, mapped) host memory, which the
+ *              kernel writes over NVLink-C2C (a serving step's result goes to
+ *              the host without a copy of its own). Pageable host memory, or a
+ *              pointer the CUDA runtime does not know, returns
+ *              MLA_ERR_INVALID_ARG before any launch.
  * Ordering: the plan part of the workspace (seq_item) is read while the kernel
  * before is still finishing, so that kernel must be the decode call that
  * produced the partials (or anything after which the plan is complete); the
@@ -353,7 +359,8 @@ mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_spl
  * array: calls whose kernels overlap on the GPU (other streams, other host
  * threads) race on it. Arguments and results
  * are those of mla_decode_paged and mla_combine (u [B][n_q][H][512] bf16,
- * lse [B][n_q][H] float or NULL). Nothing is allocated or freed. */
+ * lse [B][n_q][H] float or NULL, both in device memory). Nothing is allocated
+ * or freed. */
 size_t mla_decode_noalloc_max_bytes(void);
 mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache,
                               const int32_t* block_table, const int32_t* seq_lens,
@@ -366,7 +373,12 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache,
  *   out[t][h][v] = sum_c w_uv[h][v][c] * u[t][h][c]
  * Huny's Dev Blog section 3.2 (u_i W_i^UV after aggregation). fp32
  * accumulation, bf16 output.
- *   u [T][H][d_c] bf16, w_uv [H][d_v][d_c] bf16, out [T][H][d_v] bf16. */
+ *   u [T][H][d_c] bf16, w_uv [H][d_v][d_c] bf16, out [T][H][d_v] bf16.
+ * out may also be pinned (page-locked, mapped) host memory: the kernel then
+ * writes the rows over NVLink-C2C, so a serving step's output reaches the host
+ * without a copy of its own. Pageable host memory, or a pointer the CUDA
+ * runtime does not know, returns MLA_ERR_INVALID_ARG before any launch
+ * (checked with cudaPointerGetAttributes). */
 mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
                         int T, int H, int d_c, int d_v, void* stream);
 

@@ -505,11 +505,11 @@ class CapturedStep:
     buffers, overwritten by the next call.
 
     With ``host_io=True`` the step also owns pinned host buffers (``.host``:
-    q_nope, q_rope, block_table, seq_lens in; out, lse out), packed into one
-    input and one output area, and a second graph that copies the inputs to
-    the device in one copy, runs the step on them and copies out and lse back
-    in one copy (both copies are kernels that read or write the pinned memory,
-    ``copy16``). One serving step is then: write the new inputs into
+    q_nope, q_rope, block_table, seq_lens in, packed into one input area; out,
+    lse out), and a second graph that copies the inputs to the device in one
+    copy (a kernel that reads the pinned memory, ``copy16``) and runs the step
+    on them, with out_proj and combine writing out and lse straight into the
+    pinned buffers. One serving step is then: write the new inputs into
     ``.host``, call ``replay_host()``, synchronise the stream, read
     ``.host["out"]``. (That graph uses the block table and lengths of
     ``.host``, not the block_table / seq_lens tensors given here.)
@@ -546,8 +546,9 @@ class CapturedStep:
         self.num_splits = g
         self.host = None
         if host_io:
-            # one packed input and one packed output area, on the device and pinned
-            # on the host, so a replay moves each direction in a single copy
+            # one packed input area, on the device and pinned on the host, so a
+            # replay moves the inputs in a single copy; the outputs are written to
+            # the pinned host area by the kernels that produce them
             def layout(parts):
                 off, views = 0, {}
                 for name, shape, dtype in parts:
@@ -564,23 +565,21 @@ class CapturedStep:
                                          ("seq_lens", seq_lens.shape, torch.int32)])
             out_bytes, out_views = layout([("out", (T, H, D_V), bf), ("lse", (T, H), torch.float32)])
             self._dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
-            self._dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
             self._host_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
             self._host_out = torch.zeros(out_bytes, dtype=torch.uint8).pin_memory()
-            d_in, d_out = carve(self._dev_in, in_views), carve(self._dev_out, out_views)
+            d_in = carve(self._dev_in, in_views)
             self.host = {**carve(self._host_in, in_views), **carve(self._host_out, out_views)}
             self.host["block_table"].copy_(block_table.cpu())
             self.host["seq_lens"].copy_(seq_lens.cpu())
-            io_bufs = dict(self.bufs, out=d_out["out"], lse=d_out["lse"])
+            io_bufs = dict(self.bufs, out=self.host["out"], lse=self.host["lse"])
             io_args = (d_in["q_nope"], d_in["q_rope"], w_uk, w_uv, cache, d_in["block_table"], d_in["seq_lens"])
             io_kw = dict(kw, bufs=io_bufs)
 
-            # the packed copies run as kernels of the library (mla_copy16): the GPU
-            # reads and writes the pinned buffers itself
+            # the input copy runs as a kernel of the library (mla_copy16): the GPU
+            # reads the pinned buffer itself, as out_proj and combine write theirs
             def io_step():
                 copy16(self._host_in, self._dev_in)
                 decode_step(*io_args, **io_kw)
-                copy16(self._dev_out, self._host_out)
 
             self.graph_io = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.graph_io):
@@ -597,8 +596,8 @@ class CapturedStep:
 
     def replay_host(self):
         """One step from and to the pinned host buffers ``.host`` (``host_io=True``):
-        inputs copied in, the step, out and lse copied back, all inside one graph
-        replay on the current stream. Synchronise before reading ``.host``."""
+        inputs copied in, the step writing out and lse into ``.host``, all inside
+        one graph replay on the current stream. Synchronise before reading ``.host``."""
         if self.host is None:
             raise RuntimeError("CapturedStep was built without host_io=True")
         self.graph_io.replay()

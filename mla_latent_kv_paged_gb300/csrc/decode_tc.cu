@@ -78,8 +78,8 @@ constexpr uint32_t kTokBytes = 4 * 4;       // "partial consumed" tokens: one pe
 // ring slot, and the score readers expand it in place into the layout of the
 // 16-bit page half above (fp16 values: e4m3 converts to fp16 exactly).
 constexpr uint32_t kF8CBoxBytes = 64 * 64;   // [64 tokens][64 latent cols] e4m3
-constexpr uint32_t kF8KrBoxBytes = 64 * 32;  // [64 tokens][32 positional cols] e4m3
-constexpr uint32_t kF8StageBytes = 4 * kF8CBoxBytes + kF8KrBoxBytes;  // 18432
+constexpr uint32_t kF8KrBoxBytes = 16 * 32;  // [16 tokens][32 positional cols] e4m3, four per page half
+constexpr uint32_t kF8StageBytes = 4 * kF8CBoxBytes + 4 * kF8KrBoxBytes;  // 18432
 constexpr uint32_t kF8Off = kStageBytes - kF8StageBytes;              // 18432
 constexpr int kF8Chunks = kF8StageBytes / 16;  // 16-byte chunks of a page half: 1152
 
@@ -306,7 +306,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
     if (*reinterpret_cast<volatile int*>(&g_dbg_skip_producer)) ld.it = it1;  // load nothing
 #endif
     while (ok && ld.it < it1) {
-      const int it = ld.it;
       if (ld.pg == ld.pg0) {
         // first page of a range: the CTA's half of its query into the next two
         // ring slots (the score readers move it into tensor memory). Slot q holds
@@ -344,7 +343,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constan
 #pragma unroll
           for (int cb = 0; cb < 4; ++cb)
             tma_load_2d(dst + kF8Off + cb * kF8CBoxBytes, &map_c, fb, 256 * (int)rank + 64 * cb, y, pol_stream);
-          tma_load_2d(dst + kF8Off + 4 * kF8CBoxBytes, &map_kr, fb, kDC + 32 * (int)rank, y, pol_stream);
+          // the positional codes as four boxes of 16 rows (same bytes, same place as
+          // one box of 64 rows; measured 1.5% faster per call at 32 x 4096)
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            tma_load_2d(dst + kF8Off + 4 * kF8CBoxBytes + kb * kF8KrBoxBytes, &map_kr, fb, kDC + 32 * (int)rank,
+                        y + 16 * kb, pol_stream);
         } else {
           mbar_arrive_expect_tx(fb, kStageBytes);
 #pragma unroll
@@ -1012,7 +1016,7 @@ cudaError_t launch_decode_fp8(const uint16_t* q_abs, const uint8_t* cache8, cons
   CUtensorMap map_c, map_kr;
   const uint64_t cache_dims[2] = {kRow, (uint64_t)num_pages * page_size};
   const uint64_t row_stride[1] = {kRow};
-  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 64};
+  const uint32_t box_c[2] = {64, 64}, box_kr[2] = {32, 16};
   if (!make_tmap(&map_c, cache8, 2, cache_dims, row_stride, box_c, 0, true) ||
       !make_tmap(&map_kr, cache8, 2, cache_dims, row_stride, box_kr, 0, true))
     return cudaErrorInvalidValue;

@@ -274,9 +274,13 @@ mla_status mla_combine(const void* workspace, int B, int n_q, int H, int num_spl
     return MLA_ERR_INVALID_ARG;
   if (B < 1 || num_splits < 1) return MLA_ERR_INVALID_ARG;
   if (B > MLA_MAX_BATCH || n_q < 1 || n_q > 2 || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
+  // lse may be pinned host memory, written over the host link
+  const void* lse_dev = nullptr;
+  if (lse && !device_address(lse, &lse_dev)) return MLA_ERR_INVALID_ARG;
   Plan plan;
   plan_layout(const_cast<void*>(workspace), B, n_q, H, num_splits, &plan);
-  return launch_status(launch_combine(plan, B, n_q, H, u, lse, (cudaStream_t)stream));
+  return launch_status(launch_combine(plan, B, n_q, H, u, static_cast<float*>(const_cast<void*>(lse_dev)),
+                                      (cudaStream_t)stream));
 }
 
 mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, int T, int H,
@@ -285,7 +289,11 @@ mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out, 
   if (!aligned16(u) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
   if (T < 1) return MLA_ERR_INVALID_ARG;
   if (d_c != kDC || d_v != kDV || !heads_ok(H)) return MLA_ERR_UNSUPPORTED_SHAPE;
-  return launch_status(launch_out_proj(u, w_uv, out, T, H, (cudaStream_t)stream));
+  // out may be pinned host memory, written over the host link
+  const void* out_dev = nullptr;
+  if (!device_address(out, &out_dev)) return MLA_ERR_INVALID_ARG;
+  return launch_status(launch_out_proj(u, w_uv, static_cast<uint16_t*>(const_cast<void*>(out_dev)), T, H,
+                                       (cudaStream_t)stream));
 }
 
 mla_status mla_copy16(const void* src, void* dst, size_t bytes, void* stream) {

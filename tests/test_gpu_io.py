@@ -1,6 +1,7 @@
-"""mla_copy16, the kernel copy of a step's host I/O (GPU only): bytes from pinned host
+"""A step's host I/O (GPU only). mla_copy16, the kernel copy: bytes from pinned host
 memory to the device and back, device to device, bit for bit; pageable host memory is
-refused before any launch. Integer work: exact."""
+refused before any launch. Integer work: exact. mla_out_proj and mla_combine writing
+their outputs into pinned host memory: the bits they write into device memory."""
 import numpy as np
 import pytest
 
@@ -47,3 +48,53 @@ def test_pageable_host_memory_is_refused(mla):
     dev = torch.zeros(4096, dtype=torch.uint8, device="cuda")
     with pytest.raises(mla.MlaError):
         mla.copy16(pageable, dev)
+
+
+def _proj_inputs(T, H, seed):
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    u = (torch.randn((T, H, 512), generator=g) * 0.5).to(torch.bfloat16).cuda()
+    w_uv = (torch.randn((H, 128, 512), generator=g) / 512 ** 0.5).to(torch.bfloat16).cuda()
+    return u, w_uv
+
+
+@pytest.mark.parametrize("T", [1, 32, 77])
+def test_out_proj_writes_pinned_host_memory(mla, T):
+    """out in pinned host memory (a view at an offset inside its allocation): the bits
+    out_proj writes into device memory."""
+    import torch
+    H = 128
+    u, w_uv = _proj_inputs(T, H, 500 + T)
+    dev_out = mla.out_proj(u, w_uv)
+    pinned = torch.full((T * H * 128 + 64,), -1, dtype=torch.int16).pin_memory()
+    host_out = pinned[64:].view(torch.bfloat16).view(T, H, 128)
+    mla.out_proj(u, w_uv, host_out)
+    torch.cuda.synchronize()
+    assert torch.equal(host_out.view(torch.int16), dev_out.cpu().view(torch.int16))
+    assert torch.equal(pinned[:64], torch.full((64,), -1, dtype=torch.int16))
+
+
+def test_out_proj_refuses_pageable_host_memory(mla):
+    import torch
+    u, w_uv = _proj_inputs(4, 8, 7)
+    with pytest.raises(mla.MlaError):
+        mla.out_proj(u, w_uv, torch.zeros((4, 8, 128), dtype=torch.bfloat16))
+
+
+def test_combine_writes_lse_into_pinned_host_memory(mla):
+    import torch
+    import mla_inputs as mi
+    from tests.helpers import device_inputs
+    inp = mi.make_inputs(B=3, H=128, n_q=2, seq_lens=[70, 300, 129], seed=83)
+    pg = mi.make_paged(inp, spare_pages=4)
+    d = device_inputs(inp, pg)
+    q_abs = mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"])
+    ws, g = mla.decode_paged(q_abs, d["cache"], d["block_table"], d["seq_lens"], n_q=2, num_splits=5)
+    u_dev, lse_dev = mla.combine(ws, B=3, n_q=2, H=128, num_splits=g)
+    lse_host = torch.zeros((6, 128), dtype=torch.float32).pin_memory()
+    u2, _ = mla.combine(ws, B=3, n_q=2, H=128, num_splits=g, lse=lse_host)
+    torch.cuda.synchronize()
+    assert torch.equal(lse_host.view(torch.int32), lse_dev.cpu().view(torch.int32))
+    assert torch.equal(u2.view(torch.int16), u_dev.view(torch.int16))
+    with pytest.raises(mla.MlaError):
+        mla.combine(ws, B=3, n_q=2, H=128, num_splits=g, lse=torch.zeros((6, 128), dtype=torch.float32))
