@@ -247,8 +247,13 @@ size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);
  * the call is still finishing (in the step, mla_absorb_q): seq_lens is read
  * and the plan arrays of workspace are written in that time, so that kernel
  * must neither write seq_lens nor use workspace (for example an mla_combine
- * of an earlier call on the same workspace). q_abs, cache and block_table are
- * read after it has finished. */
+ * of an earlier call on the same workspace). With programmatic dependent
+ * launch that kernel may itself have started before the kernels ahead of it
+ * finished, so none of those may still use workspace either: a step that ends
+ * with mla_out_proj lets the next kernel start only once the whole step has
+ * finished, so consecutive such steps may share one workspace; after other
+ * sequences of calls, alternate two workspaces. q_abs, cache and block_table
+ * are read after the kernel before has finished. */
 mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                             const int32_t* block_table, const int32_t* seq_lens,
                             int B, int n_q, int H, int num_pages, int page_size,
@@ -378,7 +383,9 @@ mla_status mla_decode_noalloc(const uint16_t* q_abs, const uint16_t* cache,
  * writes the rows over NVLink-C2C, so a serving step's output reaches the host
  * without a copy of its own. Pageable host memory, or a pointer the CUDA
  * runtime does not know, returns MLA_ERR_INVALID_ARG before any launch
- * (checked with cudaPointerGetAttributes). */
+ * (checked with cudaPointerGetAttributes). The kernel enqueued after this one
+ * starts only once every kernel before this one has finished, so the next
+ * step's split plan never overlaps this step's decode kernel or merge. */
 mla_status mla_out_proj(const uint16_t* u, const uint16_t* w_uv, uint16_t* out,
                         int T, int H, int d_c, int d_v, void* stream);
 

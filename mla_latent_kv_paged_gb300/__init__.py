@@ -472,7 +472,9 @@ def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q
     """One full decode step: decode_plan -> absorb_q -> decode_paged (planned) ->
     combine -> out_proj (the plan is computed beside the kernel before it).
 
-    ``bufs`` may hold preallocated q_abs, workspace, u, lse, out tensors.
+    ``bufs`` may hold preallocated q_abs, workspace, u, lse, out tensors; steps
+    enqueued back to back may share one workspace (the step's up-projection lets
+    the next step's plan start only once the step has finished).
     Returns dict(q_abs, u, lse, out).
     """
     bufs = bufs or {}

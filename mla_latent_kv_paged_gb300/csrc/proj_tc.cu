@@ -88,10 +88,9 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
       }
     }
   }
-  // the next kernel may start now (in a decode step: after absorb_q the decode
-  // kernel, after the up-projection the next step's plan); it reads this
+  // absorb_q: the next kernel (the decode kernel) may start now; it reads this
   // kernel's output only after its own dependency wait
-  grid_launch_dependents();
+  if (kAbsorb) grid_launch_dependents();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmCols);
     tmem_relinquish();
@@ -102,6 +101,11 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   // everything above overlaps the previous kernel; its outputs are read below
   grid_dependency_wait();
+  // out_proj: the next kernel (the next step's split plan, which writes the
+  // plan part of the workspace before its own dependency wait) starts only now,
+  // when every kernel before this one has finished: none of them still reads
+  // the workspace, so consecutive steps may share one
+  if (!kAbsorb) grid_launch_dependents();
 
   const uint32_t idesc = idesc_bf16(128, C::NT, kAbsorb, false);
   auto da = [](uint32_t addr) -> uint64_t { return (uint64_t)((addr >> 4) & 0x3FFFu); };

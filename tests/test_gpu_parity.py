@@ -308,6 +308,36 @@ def test_incremental_decode_matches_fresh(mla):
             assert np.array_equal(dev_to_bits(r_fresh[k]), dev_to_bits(r_grown[k])), (L, k)
 
 
+def test_back_to_back_steps_share_one_workspace(mla):
+    """Steps enqueued back to back on one workspace with other lengths each time (so other
+    plans): the next step's plan is written while the kernel before it still runs, which
+    must not be while the previous step's decode kernel or merge still read the plan.
+    Each step is compared bit for bit with the same step run alone."""
+    import torch
+    H = 128
+    inps = [mi.make_inputs(B=8, H=H, n_q=1, seq_lens=lens, seed=90 + i)
+            for i, lens in enumerate([[4096] * 8, [64, 5000, 1, 700, 3000, 130, 2000, 900]])]
+    pgs = [mi.make_paged(x, spare_pages=2) for x in inps]
+    ds = [device_inputs(x, pg) for x, pg in zip(inps, pgs)]
+    refs = []
+    for d in ds:
+        refs.append(mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"], d["block_table"],
+                                    d["seq_lens"], n_q=1, num_splits=20))
+        torch.cuda.synchronize()
+    ws = torch.zeros(mla.workspace_bytes(8, 1, H, 20), dtype=torch.uint8, device="cuda")
+    outs = []
+    for rep in range(4):
+        for i, d in enumerate(ds):
+            outs.append((i, mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache"],
+                                            d["block_table"], d["seq_lens"], n_q=1, num_splits=20,
+                                            bufs={"workspace": ws})))
+    torch.cuda.synchronize()
+    for i, r in outs:
+        for k in ("u", "out"):
+            assert np.array_equal(dev_to_bits(r[k]), dev_to_bits(refs[i][k])), (i, k)
+        assert np.array_equal(r["lse"].cpu().numpy().view(np.uint32), refs[i]["lse"].cpu().numpy().view(np.uint32))
+
+
 def test_device_errors_are_reported_without_faulting(mla):
     import torch
     inp = mi.make_inputs(B=2, H=16, n_q=1, seq_lens=[100, 70], seed=53)
