@@ -48,3 +48,54 @@ def test_wait_runs_out_then_context_recovers():
     assert_close(dev_bf16_to_f64(r["u"]).reshape(T * H, 512), ref["u"], "u")
     assert_close(dev_bf16_to_f64(r["out"]).reshape(T * H, 128), ref["out"], "out")
     assert np.isfinite(r["lse"].cpu().numpy()).all()
+
+
+def test_fp8_wait_runs_out_then_context_recovers():
+    """The same on the FP8 cache (its own rings of code and operand slots)."""
+    import ctypes
+    import math
+
+    import torch
+
+    import mla_latent_kv_paged_gb300 as mla
+    dbg = mla.debug_lib()
+    inp = mi.make_inputs(B=2, H=128, n_q=1, seq_lens=[300, 130], seed=98)
+    pg = mi.make_paged(inp, spare_pages=2)
+    pg8 = mi.make_paged_fp8(inp, pg)
+    d = device_inputs(inp, pg)
+    cache8 = torch.from_numpy(pg8.cache).cuda()
+    scales = torch.from_numpy(pg8.scales).cuda()
+    T, H, G = inp.B * inp.n_q, inp.H, 2
+    p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    q_abs = torch.empty((T, H, 576), dtype=torch.bfloat16, device="cuda")
+    assert dbg.mla_absorb_q(p(d["q_nope"]), p(d["q_rope"]), p(d["w_uk"]), p(q_abs), T, H, 128, 64, 512, s) == 0
+    ws = torch.empty(int(dbg.mla_decode_workspace_bytes(inp.B, 1, H, G)), dtype=torch.uint8, device="cuda")
+    u = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def decode():
+        st = dbg.mla_decode_paged_fp8(p(q_abs), p(cache8), p(scales), p(d["block_table"]), p(d["seq_lens"]),
+                                      inp.B, 1, H, pg.num_pages, 64, pg.max_pages,
+                                      ctypes.c_float(1.0 / math.sqrt(192.0)), G, p(ws), ws.numel(), p(err), s)
+        assert st == 0
+        assert dbg.mla_combine(p(ws), inp.B, 1, H, G, p(u), p(lse), s) == 0
+
+    assert dbg.mla_debug_reset() == 0
+    try:
+        assert dbg.mla_debug_set_wait_limit(2_000_000) == 0
+        assert dbg.mla_debug_set_skip_producer(1) == 0
+        decode()
+        torch.cuda.synchronize()
+        assert int(err.item()) == MLA_ERR_TIMEOUT
+    finally:
+        assert dbg.mla_debug_reset() == 0
+    err.zero_()
+    decode()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    codes = mi.quantize_fp8(np.concatenate([inp.c, inp.kr], axis=1), pg8.scales)
+    ref = oracle.absorbed_fp8_f64(inp, codes, pg8.scales)
+    assert_close(dev_bf16_to_f64(u).reshape(T * H, 512), ref["u"], "u")
+    assert_close(lse.double().cpu().numpy().reshape(-1), ref["lse"], "lse")
