@@ -250,9 +250,9 @@ size_t mla_decode_workspace_bytes(int B, int n_q, int H, int num_splits);
  * of an earlier call on the same workspace). With programmatic dependent
  * launch that kernel may itself have started before the kernels ahead of it
  * finished, so none of those may still use workspace either: a step that ends
- * with mla_out_proj lets the next kernel start only once the whole step has
- * finished, so consecutive such steps may share one workspace; after other
- * sequences of calls, alternate two workspaces. q_abs, cache and block_table
+ * with mla_out_proj (or mla_out_comb) lets the next kernel start only once the
+ * whole step has finished, so consecutive such steps may share one workspace;
+ * after other sequences of calls, alternate two workspaces. q_abs, cache and block_table
  * are read after the kernel before has finished. */
 mla_status mla_decode_paged(const uint16_t* q_abs, const uint16_t* cache,
                             const int32_t* block_table, const int32_t* seq_lens,

@@ -468,10 +468,13 @@ def out_proj(u, w_uv, out=None, stream=None):
 
 def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int,
                 num_splits: int | None = None, softmax_scale: float = DEFAULT_SCALE,
-                bufs: dict | None = None, err_word=None, stream=None):
+                bufs: dict | None = None, err_word=None, stream=None, fp8_scales=None):
     """One full decode step: decode_plan -> absorb_q -> decode_paged (planned) ->
     combine -> out_proj (the plan is computed beside the kernel before it).
 
+    ``cache`` is the bf16 cache, or the FP8 cache (uint8 e4m3 codes of the same
+    shape, from ``quantize_fp8``) together with its column scales ``fp8_scales``
+    [576] float32, which the decode then reads through decode_paged_fp8.
     ``bufs`` may hold preallocated q_abs, workspace, u, lse, out tensors; steps
     enqueued back to back may share one workspace (the step's up-projection lets
     the next step's plan start only once the step has finished).
@@ -484,8 +487,15 @@ def decode_step(q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens, *, n_q
                         num_splits=num_splits, workspace=bufs.get("workspace"), err_word=err_word, stream=stream,
                         page_size=cache.shape[1])
     q_abs = absorb_q(q_nope, q_rope, w_uk, bufs.get("q_abs"), stream)
-    decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=g, softmax_scale=softmax_scale,
-                 workspace=ws, err_word=err_word, stream=stream, planned=True)
+    import torch
+    if cache.dtype == torch.uint8:
+        if fp8_scales is None:
+            raise ValueError("an FP8 cache (uint8 codes) needs its column scales fp8_scales")
+        decode_paged_fp8(q_abs, cache, fp8_scales, block_table, seq_lens, n_q=n_q, num_splits=g,
+                         softmax_scale=softmax_scale, workspace=ws, err_word=err_word, stream=stream, planned=True)
+    else:
+        decode_paged(q_abs, cache, block_table, seq_lens, n_q=n_q, num_splits=g, softmax_scale=softmax_scale,
+                     workspace=ws, err_word=err_word, stream=stream, planned=True)
     u, lse = combine(ws, B=B, n_q=n_q, H=H, num_splits=g, u=bufs.get("u"), lse=bufs.get("lse"),
                      stream=stream)
     out = out_proj(u, w_uv, bufs.get("out"), stream)
@@ -501,7 +511,8 @@ class CapturedStep:
     contents in place between calls (appending tokens, new pages) is seen by
     the next replay: the split plan is derived on the device from seq_lens
     every time. Shapes (batch, max pages per sequence, heads, n_q) and
-    num_splits are fixed at construction. Calling the object copies the new
+    num_splits are fixed at construction. An FP8 cache (uint8 codes) is given with
+    its column scales ``fp8_scales``, as for ``decode_step``. Calling the object copies the new
     queries in (from host or device tensors, asynchronously) and replays the
     graph on the current stream; the returned tensors are the step's own
     buffers, overwritten by the next call.
@@ -518,7 +529,7 @@ class CapturedStep:
     """
 
     def __init__(self, w_uk, w_uv, cache, block_table, seq_lens, *, n_q: int, num_splits: int | None = None,
-                 softmax_scale: float = DEFAULT_SCALE, err_word=None, host_io: bool = False):
+                 softmax_scale: float = DEFAULT_SCALE, err_word=None, host_io: bool = False, fp8_scales=None):
         import torch
         B = block_table.shape[0]
         H = w_uk.shape[0]
@@ -536,7 +547,8 @@ class CapturedStep:
         self.q_nope.zero_()
         self.q_rope.zero_()
         args = (self.q_nope, self.q_rope, w_uk, w_uv, cache, block_table, seq_lens)
-        kw = dict(n_q=n_q, num_splits=g, softmax_scale=softmax_scale, bufs=self.bufs, err_word=err_word)
+        kw = dict(n_q=n_q, num_splits=g, softmax_scale=softmax_scale, bufs=self.bufs, err_word=err_word,
+                  fp8_scales=fp8_scales)
         side = torch.cuda.Stream(device=dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):  # one eager run: kernel attributes, module loading

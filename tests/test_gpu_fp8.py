@@ -160,3 +160,38 @@ def test_fp8_moves_results_within_the_e4m3_bound_of_the_bf16_path(mla):
     assert mr_u <= 2.0 ** -4 and mr_out <= 2.0 ** -4 and lse_diff <= 2.0 ** -4, (mr_u, mr_out, lse_diff)
     # and it is a real change (the FP8 path does not read the bf16 cache)
     assert mr_u > 2.0 ** -9
+
+
+def test_step_and_captured_step_on_the_fp8_cache(mla):
+    """decode_step and CapturedStep take the FP8 cache with its scales: the bits of the
+    explicit FP8 path (plan, absorb, FP8 decode, merge, up-projection), and the oracle on
+    the dequantised codes."""
+    import torch
+    inp = mi.make_inputs(B=4, H=128, n_q=2, seq_lens=[3, 130, 700, 64], seed=57)
+    pg = mi.make_paged(inp, spare_pages=2)
+    d, pg8, codes = fp8_device(inp, pg, mla)
+    cache8 = torch.from_numpy(pg8.cache).cuda()
+    scales = torch.from_numpy(pg8.scales).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], cache8, d["block_table"], d["seq_lens"],
+                        n_q=2, num_splits=7, err_word=err, fp8_scales=scales)
+    q_abs = mla.absorb_q(d["q_nope"], d["q_rope"], d["w_uk"])
+    ws, g = mla.decode_paged_fp8(q_abs, cache8, scales, d["block_table"], d["seq_lens"], n_q=2, num_splits=7,
+                                 err_word=err)
+    u, lse = mla.combine(ws, B=4, n_q=2, H=128, num_splits=g)
+    out = mla.out_proj(u, d["w_uv"])
+    step = mla.CapturedStep(d["w_uk"], d["w_uv"], cache8, d["block_table"], d["seq_lens"], n_q=2, num_splits=7,
+                            err_word=err, fp8_scales=scales)
+    rc = step(d["q_nope"], d["q_rope"])
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for k, ref in (("u", u), ("out", out)):
+        assert np.array_equal(dev_to_bits(r[k]), dev_to_bits(ref)), k
+        assert np.array_equal(dev_to_bits(rc[k]), dev_to_bits(ref)), k
+    assert np.array_equal(r["lse"].cpu().numpy().view(np.uint32), lse.cpu().numpy().view(np.uint32))
+    o = oracle.absorbed_fp8_f64(inp, codes, pg8.scales)
+    T, H = inp.B * inp.n_q, inp.H
+    assert_close(dev_bf16_to_f64(r["out"]).reshape(T * H, 128), o["out"], "out")
+    with pytest.raises(ValueError):
+        mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], cache8, d["block_table"], d["seq_lens"],
+                        n_q=2)
