@@ -195,3 +195,37 @@ def test_step_and_captured_step_on_the_fp8_cache(mla):
     with pytest.raises(ValueError):
         mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], cache8, d["block_table"], d["seq_lens"],
                         n_q=2)
+
+
+def test_fp8_steps_back_to_back_on_one_workspace_and_host_io(mla):
+    """FP8 steps with alternating lengths enqueued back to back on one workspace give the bits
+    of each step run alone; the host-I/O graph on the FP8 cache gives the eager step's bits."""
+    import torch
+    inps = [mi.make_inputs(B=8, H=128, n_q=1, seq_lens=lens, seed=60 + i)
+            for i, lens in enumerate([[2048] * 8, [64, 3000, 1, 700, 2000, 130, 1500, 900]])]
+    pgs = [mi.make_paged(x, spare_pages=2) for x in inps]
+    ds = [fp8_device(x, pg, mla)[0] for x, pg in zip(inps, pgs)]
+
+    def step(d, bufs=None):
+        return mla.decode_step(d["q_nope"], d["q_rope"], d["w_uk"], d["w_uv"], d["cache8"], d["block_table"],
+                               d["seq_lens"], n_q=1, num_splits=20, bufs=bufs, fp8_scales=d["scales"])
+
+    refs = []
+    for d in ds:
+        refs.append(step(d))
+        torch.cuda.synchronize()
+    ws = torch.zeros(mla.workspace_bytes(8, 1, 128, 20), dtype=torch.uint8, device="cuda")
+    outs = [(i, step(d, {"workspace": ws})) for rep in range(3) for i, d in enumerate(ds)]
+    torch.cuda.synchronize()
+    for i, r in outs:
+        for k in ("u", "out"):
+            assert np.array_equal(dev_to_bits(r[k]), dev_to_bits(refs[i][k])), (i, k)
+    d = ds[1]
+    cap = mla.CapturedStep(d["w_uk"], d["w_uv"], d["cache8"], d["block_table"], d["seq_lens"], n_q=1,
+                           num_splits=20, host_io=True, fp8_scales=d["scales"])
+    cap.host["q_nope"].copy_(d["q_nope"].cpu())
+    cap.host["q_rope"].copy_(d["q_rope"].cpu())
+    cap.replay_host()
+    torch.cuda.synchronize()
+    assert torch.equal(cap.host["out"].view(torch.int16), refs[1]["out"].cpu().view(torch.int16))
+    assert torch.equal(cap.host["lse"], refs[1]["lse"].cpu())
