@@ -711,7 +711,7 @@ def comb_line(us, out_proj_us, T, H, hbm):
             "unmerged_weight_bytes": H * 128 * 512 * 2 + D_MODEL * H * 128 * 2, "out_proj_us": out_proj_us}
 
 
-TRAFFIC_PROFILES = {2: "decode_tc_b32_l4096.md", 4: "decode_tc_long_b4_l131072.md",
+TRAFFIC_PROFILES = {2: "decode_tc_b32_l4096.md", 3: "decode_tc_ragged_b128.md", 4: "decode_tc_long_b4_l131072.md",
                     5: "decode_tc_two_token_b64_l8192.md", "fp8": "decode_tc_fp8_b32_l4096.md"}
 
 
